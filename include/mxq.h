@@ -1,0 +1,154 @@
+/*
+ * mxq.h -- C ABI of the GB300 MX block-quantization library (libmxq.so).
+ *
+ * Plain pointers and sizes only.  Every data pointer is a DEVICE pointer that
+ * the caller owns (allocated, for example, with torch or cudaMalloc); the
+ * library never allocates, never frees and never synchronizes inside these
+ * calls.  Work is enqueued on the caller's `stream` (0 = legacy default
+ * stream), so every call can be captured in a CUDA graph and ordered with the
+ * caller's own work.
+ *
+ * Return value: MXQ_OK (0) when the work was enqueued, a negative MXQ_E* code
+ * when an argument was rejected (nothing is enqueued and no byte of any output
+ * is touched) or when the launch failed.  Argument checks run on the host and
+ * make no CUDA call, so a rejected call is safe on any thread and any device.
+ * The library never aborts, throws or raises a device trap.
+ *
+ * Checks that need device data (the group offsets of mxq_quantize_2d_dual) are
+ * made by the kernel itself: on failure it writes nothing and sets a bit in
+ * the device status word of the current device (mxq_device_status).
+ *
+ * Sources for the operations (page title, section):
+ *   [AO]  pytorch/ao PR #4995 "Fused dual-axis MXFP8 quantization with correct
+ *         metadata" -- description and review replies.
+ *   [MX9] AMD-AGI/ALTO PR #33 "mx9: add fused MX9 quantization kernel with
+ *         pack/unpack" -- Summary, "Key design choices", review thread.
+ */
+#ifndef MXQ_H_
+#define MXQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t (a repeated identical typedef
+   is legal in C11 and C++). */
+typedef struct CUstream_st *cudaStream_t;
+
+/* ---- status codes ------------------------------------------------------ */
+#define MXQ_OK 0
+#define MXQ_EBADSHAPE (-1) /* a size is negative or violates the method's multiples */
+#define MXQ_EBADDTYPE (-2) /* dtype code is not MXQ_F32 / MXQ_BF16 */
+#define MXQ_EBADOFFS (-3)  /* group count out of range, or offs/G inconsistent */
+#define MXQ_EALIGN (-4)    /* a pointer is not 16-byte aligned (offs: 4-byte) */
+#define MXQ_EOVERLAP (-5)  /* two buffers' byte ranges overlap */
+#define MXQ_ECUDA (-6)     /* the CUDA runtime refused the launch */
+#define MXQ_ENULL (-7)     /* a required pointer is NULL */
+
+/* ---- dtype codes ------------------------------------------------------- */
+#define MXQ_F32 0
+#define MXQ_BF16 1
+
+/* ---- limits ------------------------------------------------------------ */
+#define MXQ_MAX_GROUPS 1024 /* largest G accepted by mxq_quantize_2d_dual */
+
+/* ---- device status word bits (see mxq_device_status) ------------------- */
+#define MXQ_DEV_BADOFFS 0x1u /* offs failed the device-side check: no output written */
+#define MXQ_DEV_TIMEOUT 0x2u /* an internal pipeline wait gave up: outputs incomplete */
+
+/*
+ * Dual-axis MXFP8 quantization of one bf16 matrix, reading it once.
+ * [AO] description: one read of x emits four outputs -- E4M3 data cast in 1x32
+ * blocks along N (rowwise) and in 32x1 blocks along M (colwise), and the two
+ * E8M0 "rceil" scale tensors already in the blocked layout that block-scaled
+ * MMA consumes, with the colwise scales grouped by the K-group offsets and
+ * zeroed for the uncovered tail past offs[G-1].
+ *
+ *   x      bf16 [M, N] row-major (2*M*N bytes), 16-byte aligned.
+ *   M, N   multiples of 128, >= 0 ([AO]: "both dimensions and every group size
+ *          must be multiples of 128").  M == 0 or N == 0 is a no-op.
+ *   offs   device int32 [G]: cumulative group ends, non-decreasing, each a
+ *          multiple of 128, offs[G-1] <= M (empty groups allowed); 4-byte
+ *          aligned.  NULL selects dense placement (one group [0, M)); then G
+ *          must be 0.  1 <= G <= MXQ_MAX_GROUPS otherwise.
+ *   q_row  E4M3 [M*N]: q_row[m*N + n]; 16-byte aligned.
+ *   s_row  E8M0 [M*N/32]: the [M, N/32] scale matrix in the 128x4 blocked
+ *          layout: scale (r, c) at ((r/128)*(C/4) + c/4)*512 + (r%32)*16 +
+ *          ((r%128)/32)*4 + c%4 with C = N/32.
+ *   q_col  E4M3 [N*M]: q_col[n*M + m], i.e. [N, M] row-major ("logically
+ *          transposed colwise store").
+ *   s_col  E8M0 [N*M/32]: group g = [lo, hi) owns bytes [N*lo/32, N*hi/32),
+ *          its [N, (hi-lo)/32] colwise scale matrix in the same blocked
+ *          layout; bytes from N*offs[G-1]/32 to the end are written as 0.
+ *          Rows in the tail are still quantized in q_row, s_row and q_col.
+ *   stream CUDA stream for the launch.
+ * Scale and data rules ([AO] description, "Bug-compatible" list): the scale
+ * byte is the smallest s with amax <= 448*2^(s-127); data is x*2^(127-s) cast
+ * to E4M3 with round-to-nearest-even; a block with any NaN gets scale 255 and
+ * all-NaN (0x7F) data on both axes; a block with +-Inf and no NaN gets scale
+ * 255 and 0x7F data rowwise, and scale 254 with +-Inf saturated to +-448
+ * colwise.
+ * Buffers must not overlap one another, x or offs.  Every byte of every output
+ * is written (for valid offs); outputs need no initialisation.
+ */
+int mxq_quantize_2d_dual(const void *x, int64_t M, int64_t N, const int32_t *offs, int32_t G,
+                         uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                         cudaStream_t stream);
+
+/*
+ * MX9 pack.  [MX9] Summary / "Key design choices": blocks of 16 consecutive
+ * elements along the last axis (block b = r*(cols/16) + j); per block a
+ * shared exponent E = max over the block of the element exponents taken from
+ * the native bits (biased exponent field - 127: fp32 bits 30..23, bf16 bits
+ * 14..7), stored as max_exp[b] = E + 127; per pair p of elements (2p, 2p+1) a
+ * prime bit (bit p of prime[b], LSB = pair 0) set when the pair's exponent is
+ * below E; scale exponent k_p = max(E - 6 - prime_p, -126); data
+ * q = clamp(round_half_even(x / 2^k_p), -127, 127).  NaN packs to 0, +-Inf to
+ * +-127 (max_exp 255).
+ *
+ *   x        fp32 or bf16 [rows, cols] row-major, 16-byte aligned.
+ *   dtype    MXQ_F32 or MXQ_BF16 (type of x).
+ *   rows, cols  rows >= 0, cols >= 0 and cols % 16 == 0.
+ *   q        int8 [n_blocks, 16], n_blocks = rows*cols/16; 16-byte aligned.
+ *   max_exp  uint8 [n_blocks].
+ *   prime    uint8 [n_blocks] (the page's [n_blocks, 1]).
+ * Buffers must not overlap.  9 bits per element in total.
+ */
+int mx9_pack(const void *x, int dtype, int64_t rows, int64_t cols, int8_t *q, uint8_t *max_exp,
+             uint8_t *prime, cudaStream_t stream);
+
+/*
+ * MX9 unpack: y = q * 2^k_p with k_p rebuilt from max_exp and prime as in
+ * mx9_pack ([MX9] Summary: the packed form is dequantized back to fp32/bf16;
+ * the caller passes the shape back because it is not stored).  The result is
+ * exact in fp32 and bf16; a block with max_exp 255 can give +-Inf.
+ *
+ *   q, max_exp, prime  as produced by mx9_pack (q 16-byte aligned).
+ *   y        fp32 or bf16 [rows, cols] row-major output, 16-byte aligned.
+ *   dtype    MXQ_F32 or MXQ_BF16 (type of y).
+ */
+int mx9_unpack(const int8_t *q, const uint8_t *max_exp, const uint8_t *prime, void *y, int dtype,
+               int64_t rows, int64_t cols, cudaStream_t stream);
+
+/*
+ * Device status word of the current device: a sticky OR of MXQ_DEV_* bits set
+ * by kernels since the last clear.  Writes it to *out and clears it when
+ * `clear` is non-zero.  This call synchronizes the device (it reads device
+ * memory); use it for diagnostics and tests, not inside captured work.
+ * Returns MXQ_OK, MXQ_ENULL or MXQ_ECUDA.
+ */
+int mxq_device_status(uint32_t *out, int clear);
+
+/* Static description of a status code (never NULL). */
+const char *mxq_status_string(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+int mxq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H_ */

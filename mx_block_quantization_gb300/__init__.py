@@ -1,0 +1,229 @@
+"""GB300-native MX block quantization: a thin Python binding over libmxq.so.
+
+The binding only marshals torch tensors into the C ABI declared in
+``include/mxq.h``; every step of the computation runs in the library's sm_103a
+kernels.  There is no CPU fallback: calling an op without the built library,
+or with tensors that are not on a CUDA device, raises.
+
+Operations (sources by page title):
+
+* :func:`quantize_2d_dual` -- pytorch/ao PR #4995 "Fused dual-axis MXFP8
+  quantization with correct metadata": one read of a bf16 [M, N] tensor gives
+  rowwise (1x32) and colwise (32x1) E4M3 data and both E8M0 rceil scale
+  tensors in the 128x4 blocked layout, colwise scales per K-group slab with
+  the tail past offs[-1] zeroed.
+* :func:`mx9_pack` / :func:`mx9_unpack` -- AMD-AGI/ALTO PR #33 "mx9: add fused
+  MX9 quantization kernel with pack/unpack": block 16, int8 q in [-127, 127],
+  E8M0 shared exponent, one prime bit per pair.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import NamedTuple, Optional
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libmxq.so"
+
+# status codes and constants of mxq.h
+OK = 0
+EBADSHAPE = -1
+EBADDTYPE = -2
+EBADOFFS = -3
+EALIGN = -4
+EOVERLAP = -5
+ECUDA = -6
+ENULL = -7
+F32 = 0
+BF16 = 1
+MAX_GROUPS = 1024
+DEV_BADOFFS = 0x1
+DEV_TIMEOUT = 0x2
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class MxqError(RuntimeError):
+    """A call into libmxq.so returned a non-zero status."""
+
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxq.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise ImportError(
+                f"{LIB_PATH.name} is not built; run `python -c 'import __graft_entry__ as g; "
+                f"g.build()'` (there is no CPU fallback)")
+        L = ctypes.CDLL(str(LIB_PATH))
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        L.mxq_quantize_2d_dual.restype = ctypes.c_int
+        L.mxq_quantize_2d_dual.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+        L.mx9_pack.restype = ctypes.c_int
+        L.mx9_pack.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
+        L.mx9_unpack.restype = ctypes.c_int
+        L.mx9_unpack.argtypes = [vp, vp, vp, vp, ctypes.c_int, i64, i64, vp]
+        L.mxq_device_status.restype = ctypes.c_int
+        L.mxq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        L.mxq_status_string.restype = ctypes.c_char_p
+        L.mxq_status_string.argtypes = [ctypes.c_int]
+        L.mxq_version.restype = ctypes.c_int
+        L.mxq_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().mxq_status_string(int(code)).decode()
+
+
+def version() -> tuple[int, int]:
+    v = lib().mxq_version()
+    return v >> 16, v & 0xFFFF
+
+
+def device_status(clear: bool = True) -> int:
+    """Sticky MXQ_DEV_* bits of the current device (synchronizes the device)."""
+    out = ctypes.c_uint32(0)
+    rc = lib().mxq_device_status(ctypes.byref(out), int(bool(clear)))
+    if rc != OK:
+        raise MxqError(rc, "mxq_device_status")
+    return int(out.value)
+
+
+# ---------------------------------------------------------------------------
+# torch-facing wrappers (marshalling only)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check_cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(device, stream):
+    torch = _torch()
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class DualOutputs(NamedTuple):
+    q_row: "object"  # uint8 [M, N]    E4M3 bytes, 1x32 blocks along N
+    s_row: "object"  # uint8 [M*N/32]  E8M0, blocked [M, N/32]
+    q_col: "object"  # uint8 [N, M]    E4M3 bytes, 32x1 blocks along M, transposed
+    s_col: "object"  # uint8 [N*M/32]  E8M0, per-group blocked slabs, zero tail
+
+
+def quantize_2d_dual(x, offs=None, *, out: Optional[DualOutputs] = None, stream=None) -> DualOutputs:
+    """Dual-axis MXFP8 cast of a bf16 CUDA tensor [M, N] (M, N multiples of 128).
+
+    ``offs``: optional int32 CUDA tensor of cumulative group ends (multiples of
+    128, non-decreasing, offs[-1] <= M); None means one dense group.
+    Returns uint8 tensors; view them as torch.float8_e4m3fn / float8_e8m0fnu as
+    needed.  An invalid ``offs`` is detected on the device: nothing is written
+    and :func:`device_status` reports DEV_BADOFFS.
+    """
+    torch = _torch()
+    _check_cuda(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    M, N = x.shape
+    G = 0
+    if offs is not None:
+        _check_cuda(offs, "offs")
+        if offs.dtype != torch.int32 or offs.dim() != 1:
+            raise ValueError("offs must be a 1-D int32 tensor")
+        if offs.device != x.device:
+            raise ValueError("offs must be on x's device")
+        G = offs.numel()
+    if out is None:
+        kw = dict(dtype=torch.uint8, device=x.device)
+        out = DualOutputs(torch.empty((M, N), **kw), torch.empty((M * N // 32,), **kw),
+                          torch.empty((N, M), **kw), torch.empty((N * M // 32,), **kw))
+    for name, t, n in zip(DualOutputs._fields, out, (M * N, M * N // 32, M * N, M * N // 32)):
+        _check_cuda(t, name)
+        if t.dtype != torch.uint8 or t.numel() != n or t.device != x.device:
+            raise ValueError(f"{name} must be a uint8 tensor of {n} elements on x's device")
+    with torch.cuda.device(x.device):
+        rc = lib().mxq_quantize_2d_dual(
+            ctypes.c_void_p(x.data_ptr()), M, N,
+            ctypes.c_void_p(offs.data_ptr() if offs is not None else 0), G,
+            *(ctypes.c_void_p(t.data_ptr()) for t in out), _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_quantize_2d_dual")
+    return out
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise ValueError("dtype must be float32 or bfloat16")
+
+
+def mx9_pack(x, *, out=None, stream=None):
+    """MX9 pack of a fp32/bf16 CUDA tensor [rows, cols], cols % 16 == 0.
+
+    Returns (q int8 [n_blocks, 16], max_exp uint8 [n_blocks], prime uint8 [n_blocks, 1]).
+    """
+    torch = _torch()
+    _check_cuda(x, "x")
+    dt = _dtype_code(x)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    rows, cols = x.shape
+    nb = rows * cols // 16
+    if out is None:
+        out = (torch.empty((nb, 16), dtype=torch.int8, device=x.device),
+               torch.empty((nb,), dtype=torch.uint8, device=x.device),
+               torch.empty((nb, 1), dtype=torch.uint8, device=x.device))
+    q, e, p = out
+    for name, t, dtype, n in (("q", q, torch.int8, nb * 16), ("max_exp", e, torch.uint8, nb),
+                              ("prime", p, torch.uint8, nb)):
+        _check_cuda(t, name)
+        if t.dtype != dtype or t.numel() != n or t.device != x.device:
+            raise ValueError(f"{name}: expected {dtype} with {n} elements on x's device")
+    with torch.cuda.device(x.device):
+        rc = lib().mx9_pack(ctypes.c_void_p(x.data_ptr()), dt, rows, cols,
+                            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(e.data_ptr()),
+                            ctypes.c_void_p(p.data_ptr()), _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mx9_pack")
+    return q, e, p
+
+
+def mx9_unpack(q, max_exp, prime, out_dtype, shape, *, out=None, stream=None):
+    """Rebuild a [rows, cols] fp32/bf16 CUDA tensor from the MX9 parts (shape is passed back)."""
+    torch = _torch()
+    rows, cols = shape
+    nb = rows * cols // 16
+    for name, t, dtype, n in (("q", q, torch.int8, nb * 16), ("max_exp", max_exp, torch.uint8, nb),
+                              ("prime", prime, torch.uint8, nb)):
+        _check_cuda(t, name)
+        if t.dtype != dtype or t.numel() != n or t.device != q.device:
+            raise ValueError(f"{name}: expected {dtype} with {n} elements on q's device")
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype, device=q.device)
+    _check_cuda(out, "out")
+    if out.dtype != out_dtype or out.numel() != rows * cols or out.device != q.device:
+        raise ValueError("out must match out_dtype, shape and q's device")
+    dt = _dtype_code(out)
+    with torch.cuda.device(q.device):
+        rc = lib().mx9_unpack(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(max_exp.data_ptr()),
+                              ctypes.c_void_p(prime.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                              dt, rows, cols, _stream_handle(q.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mx9_unpack")
+    return out

@@ -1,0 +1,496 @@
+// mxq_dual.cu -- one-pass dual-axis MXFP8 quantization for sm_103a.
+//
+// Method: pytorch/ao PR #4995 "Fused dual-axis MXFP8 quantization with
+// correct metadata" (description): read a bf16 [M, N] tensor once and emit
+// E4M3 data cast in 1x32 blocks along N and in 32x1 blocks along M (stored
+// transposed), plus both E8M0 rceil scale tensors already in the 128x4
+// blocked layout of block-scaled MMA, the colwise scales placed per K-group
+// slab and zeroed past offs[G-1].
+//
+// GB300 design (a persistent, warp-specialized, bandwidth-bound kernel; no
+// tensor cores because there is no contraction):
+//   * one CTA per SM walks 128x128 tiles t = blockIdx.x + k * gridDim.x;
+//   * warp 16 (producer) streams tiles into a 4-stage shared-memory ring with
+//     2-D TMA loads (two 64-column boxes per tile, 128-byte swizzle);
+//   * warps 0..15 (consumers) run the rowwise and the colwise pass of a tile
+//     from shared memory and write its four outputs into a double-buffered
+//     shared staging area (E4M3 tiles in the same 128-byte swizzle, 512-byte
+//     scale atoms already in blocked order);
+//   * warp 17 (storer) drains each staged tile with two TMA tensor stores
+//     (q_row, q_col) and two 512-byte bulk stores (the s_row atom and either
+//     the s_col atom at its group slab or a zero atom for tail rows).
+// Every pipeline wait is bounded; on a timeout the CTA raises a status bit,
+// drains the copies it has in flight and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "mxq.h"
+#include "mxq_device.cuh"
+#include "mxq_host.h"
+
+namespace {
+
+using namespace mxq;
+
+constexpr int kTile = 128;
+constexpr int kStages = 4;
+constexpr int kConsumerWarps = 16;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kStoreWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;  // 576
+
+constexpr uint32_t kInStageBytes = kTile * kTile * 2;  // bf16 tile, 32 KiB
+constexpr uint32_t kHalfBytes = kTile * 64 * 2;        // [128 rows][64 bf16] box, 16 KiB
+constexpr uint32_t kQTileBytes = kTile * kTile;        // E4M3 tile, 16 KiB
+constexpr uint32_t kAtomBytes = 512;                   // one 128x4 scale atom
+
+// Shared-memory map (offsets from a 1024-byte aligned base; every swizzled
+// buffer starts on a 1024-byte boundary as the 128-byte swizzle requires).
+constexpr uint32_t kOffIn = 0;
+constexpr uint32_t kOffQRow = kOffIn + kStages * kInStageBytes;
+constexpr uint32_t kOffQCol = kOffQRow + 2 * kQTileBytes;
+constexpr uint32_t kOffSRow = kOffQCol + 2 * kQTileBytes;
+constexpr uint32_t kOffSCol = kOffSRow + 2 * kAtomBytes;
+constexpr uint32_t kOffZero = kOffSCol + 2 * kAtomBytes;
+constexpr uint32_t kOffOffs = kOffZero + kAtomBytes;
+constexpr uint32_t kOffBar = kOffOffs + 4 * MXQ_MAX_GROUPS;
+constexpr uint32_t kNumBars = 2 * kStages + 4;
+constexpr uint32_t kOffFlag = kOffBar + 8 * kNumBars;
+constexpr uint32_t kSmemUsed = kOffFlag + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kOffQRow % 1024 == 0 && kOffQCol % 1024 == 0, "swizzle alignment");
+
+// Sticky per-device status word (MXQ_DEV_* bits), read by mxq_device_status.
+__device__ unsigned int g_mxq_status = 0;
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (kStages + s); }
+  __device__ uint32_t ofull(int b) const { return base + 8u * (2 * kStages + b); }
+  __device__ uint32_t oempty(int b) const { return base + 8u * (2 * kStages + 2 + b); }
+};
+
+// Physical byte offset of 16-byte chunk `chunk` of row `row` in a buffer of
+// 128-byte rows written with the 128-byte TMA swizzle (chunk ^= row % 8).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// Rowwise pass: thread (r, j) quantizes the 1x32 block j of tile row r.
+// Warp w owns rows 8w..8w+7; lane l takes row 8w + l/4 and block l%4.
+// Block j lives in half-tile j/2, logical chunks (j%2)*4 .. +3.  Lanes with
+// j >= 2 read their four chunks rotated by two so that each 8-lane phase of
+// the 128-bit loads touches eight distinct bank groups; the rotation swaps
+// which 16-byte half of the output each half of the registers feeds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void rowwise_pass(uint32_t in_s, uint32_t qrow_s, uint32_t srow_s,
+                                             int warp, int lane) {
+  const int r = warp * 8 + (lane >> 2);
+  const int j = lane & 3;
+  const int rot = (j >> 1) * 2;
+  const uint32_t half = in_s + static_cast<uint32_t>(j >> 1) * kHalfBytes;
+
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int chunk = (j & 1) * 4 + ((k + rot) & 3);
+    const uint4 v = lds128(half + swz(r, chunk));
+    w[4 * k + 0] = v.x;
+    w[4 * k + 1] = v.y;
+    w[4 * k + 2] = v.z;
+    w[4 * k + 3] = v.w;
+  }
+
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  const uint32_t amax = max(m & 0xFFFFu, m >> 16);
+  const uint32_t s = e8m0_rceil_from_bits(amax, 255u);
+  const float mult = e8m0_multiplier(s);
+
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = w[2 * i], b = w[2 * i + 1];
+    const uint32_t lo = cvt_e4m3x2(fmul_rn_noftz(bf16_hi_f32(a), mult),
+                                   fmul_rn_noftz(bf16_lo_f32(a), mult));
+    const uint32_t hi = cvt_e4m3x2(fmul_rn_noftz(bf16_hi_f32(b), mult),
+                                   fmul_rn_noftz(bf16_lo_f32(b), mult));
+    o[i] = (s == 255u) ? 0x7F7F7F7Fu : (lo | (hi << 16));
+  }
+  // registers o[0..3] hold block bytes (rot ? 16..31 : 0..15), o[4..7] the rest
+  const int first = 2 * j + (rot ? 1 : 0);
+  const int second = 2 * j + (rot ? 0 : 1);
+  sts128(qrow_s + swz(r, first), o[0], o[1], o[2], o[3]);
+  sts128(qrow_s + swz(r, second), o[4], o[5], o[6], o[7]);
+  // scale (r, j) of this tile's 128x4 atom
+  sts8(srow_s + static_cast<uint32_t>((r & 31) * 16 + (r >> 5) * 4 + j), s);
+}
+
+// ---------------------------------------------------------------------------
+// Colwise pass: warp w takes row block i = w/4 (rows 32i..32i+31) and the 32
+// columns 32*(w%4)..+31; lane l takes column pair p = 16*(w%4) + l%16
+// (columns 2p, 2p+1) over rows 32i + 16*(l/16) .. +15.  The two 16-row halves
+// combine their amax with one shuffle.  Lanes of the upper half visit their
+// rows with the 4-row groups swapped (row index j ^ 4) so that the two halves
+// of each 32-bit load hit different bank groups; the swap is undone when the
+// output words are placed.  E4M3 bytes for four consecutive rows of one
+// column are packed into one word, so each lane emits two 16-byte runs of
+// q_col (one per column), written with the swizzle into the [n][m] tile.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void colwise_pass(uint32_t in_s, uint32_t qcol_s, uint32_t scol_s,
+                                             int warp, int lane) {
+  const int i = warp >> 2;
+  const int cg = warp & 3;
+  const int pl = lane & 15;
+  const int rh = lane >> 4;
+  const int p = cg * 16 + pl;
+  const uint32_t half = in_s + static_cast<uint32_t>(cg >> 1) * kHalfBytes;
+  const int chunk = (p & 31) >> 2;
+  const uint32_t within = static_cast<uint32_t>(p & 3) * 4u;
+
+  uint32_t w[16];
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    const int row = 32 * i + 16 * rh + (jj ^ (4 * rh));
+    w[jj] = lds32(half + swz(row, chunk) + within);
+  }
+
+  uint32_t m = 0;
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) m = __vmaxu2(m, w[jj] & 0x7FFF7FFFu);
+  m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+  const uint32_t s_lo = e8m0_rceil_from_bits(m & 0xFFFFu, 254u);  // column 2p
+  const uint32_t s_hi = e8m0_rceil_from_bits(m >> 16, 254u);      // column 2p+1
+  const float mult_lo = e8m0_multiplier(s_lo);
+  const float mult_hi = e8m0_multiplier(s_hi);
+
+  // c_lo[g] / c_hi[g]: rows 4g..4g+3 (register order) of column 2p / 2p+1
+  uint32_t c_lo[4], c_hi[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t a = w[4 * g], b = w[4 * g + 1], c = w[4 * g + 2], d = w[4 * g + 3];
+    const uint32_t l01 = cvt_e4m3x2(fmul_rn_noftz(bf16_lo_f32(b), mult_lo),
+                                    fmul_rn_noftz(bf16_lo_f32(a), mult_lo));
+    const uint32_t l23 = cvt_e4m3x2(fmul_rn_noftz(bf16_lo_f32(d), mult_lo),
+                                    fmul_rn_noftz(bf16_lo_f32(c), mult_lo));
+    const uint32_t h01 = cvt_e4m3x2(fmul_rn_noftz(bf16_hi_f32(b), mult_hi),
+                                    fmul_rn_noftz(bf16_hi_f32(a), mult_hi));
+    const uint32_t h23 = cvt_e4m3x2(fmul_rn_noftz(bf16_hi_f32(d), mult_hi),
+                                    fmul_rn_noftz(bf16_hi_f32(c), mult_hi));
+    c_lo[g] = (s_lo == 255u) ? 0x7F7F7F7Fu : (l01 | (l23 << 16));
+    c_hi[g] = (s_hi == 255u) ? 0x7F7F7F7Fu : (h01 | (h23 << 16));
+  }
+  // undo the 4-row-group swap of the upper half: output group G is c[G ^ rh]
+  const bool sw = rh != 0;
+  const uint32_t L0 = sw ? c_lo[1] : c_lo[0], L1 = sw ? c_lo[0] : c_lo[1];
+  const uint32_t L2 = sw ? c_lo[3] : c_lo[2], L3 = sw ? c_lo[2] : c_lo[3];
+  const uint32_t H0 = sw ? c_hi[1] : c_hi[0], H1 = sw ? c_hi[0] : c_hi[1];
+  const uint32_t H2 = sw ? c_hi[3] : c_hi[2], H3 = sw ? c_hi[2] : c_hi[3];
+
+  const int n_lo = 2 * p, n_hi = 2 * p + 1;  // tile-local columns = q_col tile rows
+  const int mchunk = 2 * i + rh;             // 16-byte run of rows within the 128
+  const uint32_t a_lo = qcol_s + swz(n_lo, mchunk);
+  const uint32_t a_hi = qcol_s + swz(n_hi, mchunk);
+  if ((pl & 7) < 4) {
+    sts128(a_lo, L0, L1, L2, L3);
+    sts128(a_hi, H0, H1, H2, H3);
+  } else {
+    sts128(a_hi, H0, H1, H2, H3);
+    sts128(a_lo, L0, L1, L2, L3);
+  }
+  if (rh == 0) {
+    sts8(scol_s + static_cast<uint32_t>((n_lo & 31) * 16 + (n_lo >> 5) * 4 + i), s_lo);
+    sts8(scol_s + static_cast<uint32_t>((n_hi & 31) * 16 + (n_hi >> 5) * 4 + i), s_hi);
+  }
+}
+
+// First g with offs[g] > row (the group holding `row`), by binary search.
+__device__ __forceinline__ int group_of_row(const int32_t* s_offs, int G, int64_t row) {
+  int lo = 0, hi = G;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(s_offs[mid]) > row)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mxq_dual_kernel(const __grid_constant__ CUtensorMap tm_x,
+                    const __grid_constant__ CUtensorMap tm_qrow,
+                    const __grid_constant__ CUtensorMap tm_qcol, const int32_t* __restrict__ offs,
+                    int G, int M, int N, uint8_t* __restrict__ s_row,
+                    uint8_t* __restrict__ s_col) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t TN = N / kTile;
+  const int64_t T = static_cast<int64_t>(M / kTile) * TN;
+  const int64_t my_tiles =
+      (static_cast<int64_t>(blockIdx.x) < T) ? (T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  const Bars bars{base + kOffBar};
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kOffFlag);
+  int32_t* s_offs = reinterpret_cast<int32_t*>(gbase + kOffOffs);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), kConsumerWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.ofull(b), kConsumerWarps);
+      mbar_init(bars.oempty(b), 1);
+    }
+    *abort_flag = 0u;
+    mbar_init_fence();
+  }
+  if (tid < kAtomBytes / 4) {
+    sts32(base + kOffZero + 4u * tid, 0u);
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  // Producer prologue: start the first loads before the offsets check.
+  int64_t issued = 0;
+  const bool is_producer = (warp == kProducerWarp) && (lane == 0);
+  auto issue_load = [&](int64_t k) {
+    const int64_t t = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
+    const int32_t ti = static_cast<int32_t>(t / TN), tj = static_cast<int32_t>(t % TN);
+    const int s = static_cast<int>(k % kStages);
+    const uint32_t dst = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
+    mbar_arrive_expect_tx(bars.full(s), kInStageBytes);
+    tma_load_2d(dst, &tm_x, tj * kTile, ti * kTile, bars.full(s));
+    tma_load_2d(dst + kHalfBytes, &tm_x, tj * kTile + 64, ti * kTile, bars.full(s));
+  };
+  auto drain_loads = [&]() {
+    for (int64_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
+      mbar_wait_drain(bars.full(static_cast<int>(k % kStages)),
+                      static_cast<uint32_t>((k / kStages) & 1));
+  };
+  if (is_producer) {
+    tma_prefetch_desc(&tm_x);
+    for (; issued < my_tiles && issued < kStages; ++issued) issue_load(issued);
+  }
+
+  // Device-side check of the group offsets: ascending, multiples of 128,
+  // within [0, M].  Every CTA reaches the same verdict; on failure nothing is
+  // written and the status word records it.
+  int64_t end_rows = M;
+  if (offs != nullptr) {
+    int bad = 0;
+    for (int g = tid; g < G; g += kThreads) {
+      const int32_t v = offs[g];
+      const int32_t prev = g ? offs[g - 1] : 0;
+      if (v < prev || (v & (kTile - 1)) != 0 || v > M) bad = 1;
+      s_offs[g] = v;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+      if (blockIdx.x == 0 && tid == 0) atomicOr(&g_mxq_status, MXQ_DEV_BADOFFS);
+      if (is_producer) drain_loads();
+      return;
+    }
+    end_rows = s_offs[G - 1];
+  }
+
+  if (warp < kConsumerWarps) {
+    // ------------------------------------------------------------- consumers
+    for (int64_t k = 0; k < my_tiles; ++k) {
+      const int s = static_cast<int>(k % kStages);
+      const int b = static_cast<int>(k & 1);
+      // every lane waits (acquiring the barrier's data); the warp leaves
+      // together if any lane gave up, so no warp-collective runs short
+      bool ok = mbar_wait_bounded(bars.full(s), static_cast<uint32_t>((k / kStages) & 1),
+                                  abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT);
+      if (ok && k >= 2)
+        ok = mbar_wait_bounded(bars.oempty(b), static_cast<uint32_t>(((k >> 1) - 1) & 1),
+                               abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return;
+      const uint32_t in_s = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
+      rowwise_pass(in_s, base + kOffQRow + b * kQTileBytes, base + kOffSRow + b * kAtomBytes, warp,
+                   lane);
+      colwise_pass(in_s, base + kOffQCol + b * kQTileBytes, base + kOffSCol + b * kAtomBytes, warp,
+                   lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.empty(s));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.ofull(b));
+    }
+  } else if (warp == kProducerWarp) {
+    // -------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int64_t k = issued; k < my_tiles; ++k) {
+        const int s = static_cast<int>(k % kStages);
+        if (!mbar_wait_bounded(bars.empty(s), static_cast<uint32_t>(((k / kStages) - 1) & 1),
+                               abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT)) {
+          drain_loads();
+          return;
+        }
+        issue_load(k);
+        issued = k + 1;
+      }
+    }
+  } else if (warp == kStoreWarp) {
+    // ---------------------------------------------------------------- storer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_qrow);
+      tma_prefetch_desc(&tm_qcol);
+      const int64_t Mrows = M;
+      for (int64_t k = 0; k < my_tiles; ++k) {
+        const int b = static_cast<int>(k & 1);
+        if (!mbar_wait_bounded(bars.ofull(b), static_cast<uint32_t>((k >> 1) & 1), abort_flag,
+                               &g_mxq_status, MXQ_DEV_TIMEOUT))
+          break;
+        const int64_t t = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
+        const int64_t ti = t / TN, tj = t % TN;
+        const int64_t row0 = ti * kTile;
+        tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
+                     base + kOffQRow + b * kQTileBytes);
+        tma_store_2d(&tm_qcol, static_cast<int32_t>(row0), static_cast<int32_t>(tj * kTile),
+                     base + kOffQCol + b * kQTileBytes);
+        bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
+                   kAtomBytes);
+        if (row0 < end_rows) {
+          int64_t lo = 0, hi = Mrows;
+          if (offs != nullptr) {
+            const int g = group_of_row(s_offs, G, row0);
+            lo = g ? s_offs[g - 1] : 0;
+            hi = s_offs[g];
+          }
+          const int64_t atoms_per_nblock = (hi - lo) / kTile;  // (hi-lo)/32 scale cols / 4
+          uint8_t* dst = s_col + static_cast<int64_t>(N) * lo / 32 +
+                         (tj * atoms_per_nblock + (row0 - lo) / kTile) * kAtomBytes;
+          bulk_store(dst, base + kOffSCol + b * kAtomBytes, kAtomBytes);
+        } else {
+          uint8_t* dst = s_col + static_cast<int64_t>(N) * end_rows / 32 +
+                         (((row0 - end_rows) / kTile) * TN + tj) * kAtomBytes;
+          bulk_store(dst, base + kOffZero, kAtomBytes);
+        }
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(bars.oempty(b));
+      }
+      bulk_wait_all<0>();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool ensure_dual_smem_attr(int dev) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  if (dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(mxq_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return false;
+    done[dev] = true;
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" int mxq_quantize_2d_dual(const void* x, int64_t M, int64_t N, const int32_t* offs,
+                                    int32_t G, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                                    uint8_t* s_col, cudaStream_t stream) {
+  if (M < 0 || N < 0 || M % kTile != 0 || N % kTile != 0 || M > INT32_MAX || N > INT32_MAX)
+    return MXQ_EBADSHAPE;
+  if (offs == nullptr ? G != 0 : (G < 1 || G > MXQ_MAX_GROUPS)) return MXQ_EBADOFFS;
+  if (offs != nullptr && !aligned_to(offs, 4)) return MXQ_EALIGN;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!x || !q_row || !s_row || !q_col || !s_col) return MXQ_ENULL;
+  if (!aligned_to(x, 16) || !aligned_to(q_row, 16) || !aligned_to(s_row, 16) ||
+      !aligned_to(q_col, 16) || !aligned_to(s_col, 16))
+    return MXQ_EALIGN;
+  const uint64_t MN = static_cast<uint64_t>(M) * static_cast<uint64_t>(N);
+  const ByteRange r[6] = {
+      {reinterpret_cast<uintptr_t>(x), 2 * MN},
+      {reinterpret_cast<uintptr_t>(q_row), MN},
+      {reinterpret_cast<uintptr_t>(q_col), MN},
+      {reinterpret_cast<uintptr_t>(s_row), MN / 32},
+      {reinterpret_cast<uintptr_t>(s_col), MN / 32},
+      {reinterpret_cast<uintptr_t>(offs), offs ? 4ull * static_cast<uint64_t>(G) : 0ull},
+  };
+  if (ranges_overlap(r, 6)) return MXQ_EOVERLAP;
+
+  int dev = 0;
+  const int sms = sm_count_current_device(&dev);
+  if (sms <= 0 || !ensure_dual_smem_attr(dev)) return MXQ_ECUDA;
+
+  CUtensorMap tm_x, tm_qrow, tm_qcol;
+  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, N, M, 2ull * N, 64, kTile) ||
+      !encode_2d(&tm_qrow, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, N, M, N, kTile, kTile) ||
+      !encode_2d(&tm_qcol, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, M, N, M, kTile, kTile))
+    return MXQ_ECUDA;
+
+  const int64_t T = (M / kTile) * (N / kTile);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T < sms ? T : sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, mxq_dual_kernel, tm_x, tm_qrow, tm_qcol, offs, static_cast<int>(G),
+                         static_cast<int>(M), static_cast<int>(N), s_row, s_col);
+  return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
+}
+
+extern "C" int mxq_device_status(uint32_t* out, int clear) {
+  if (!out) return MXQ_ENULL;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mxq_status, sizeof v) != cudaSuccess) return MXQ_ECUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_mxq_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ECUDA;
+  }
+  *out = v;
+  return MXQ_OK;
+}

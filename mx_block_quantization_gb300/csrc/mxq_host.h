@@ -1,0 +1,54 @@
+// mxq_host.h -- host-side argument checks and device queries shared by the
+// launch code.  Nothing here calls CUDA except the device-property helpers,
+// which are only reached after every argument check has passed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "mxq.h"
+
+namespace mxq {
+
+inline bool aligned_to(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// A byte range [lo, lo + bytes) of one buffer; empty ranges never overlap.
+struct ByteRange {
+  uintptr_t lo;
+  uint64_t bytes;
+};
+
+inline bool ranges_overlap(const ByteRange* r, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (r[i].bytes == 0) continue;
+    for (int j = i + 1; j < n; ++j) {
+      if (r[j].bytes == 0) continue;
+      const uintptr_t a0 = r[i].lo, a1 = r[i].lo + r[i].bytes;
+      const uintptr_t b0 = r[j].lo, b1 = r[j].lo + r[j].bytes;
+      if (a0 < b1 && b0 < a1) return true;
+    }
+  }
+  return false;
+}
+
+// Number of SMs of the current device, cached per device ordinal.
+inline int sm_count_current_device(int* out_device) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (out_device) *out_device = dev;
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace mxq

@@ -1,0 +1,128 @@
+"""The C ABI library loads, exports every function declared in include/mxq.h, and
+rejects bad arguments on the host (these paths make no CUDA call, so they run
+without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mx_block_quantization_gb300 as mxq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not mxq.LIB_PATH.exists():
+        import __graft_entry__
+        __graft_entry__.build()
+    return mxq.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared_functions())
+    assert {"mxq_quantize_2d_dual", "mx9_pack", "mx9_unpack", "mxq_device_status",
+            "mxq_status_string", "mxq_version"} <= names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    for code in (mxq.OK, mxq.EBADSHAPE, mxq.EBADDTYPE, mxq.EBADOFFS, mxq.EALIGN, mxq.EOVERLAP,
+                 mxq.ECUDA, mxq.ENULL):
+        s = mxq.status_string(code)
+        assert s and s != "unknown status"
+    assert mxq.status_string(12345) == "unknown status"
+    assert mxq.version() == (1, 0)
+
+
+A = 1 << 20  # fake, 16-byte aligned "device addresses": never dereferenced
+
+
+def _dual(L, x=A, M=128, N=128, offs=None, G=0, qr=None, sr=None, qc=None, sc=None):
+    MN = M * N
+    qr = A + 4 * MN if qr is None else qr
+    qc = A + 8 * MN if qc is None else qc
+    sr = A + 12 * MN if sr is None else sr
+    sc = A + 14 * MN if sc is None else sc
+    return L.mxq_quantize_2d_dual(ctypes.c_void_p(x), M, N, ctypes.c_void_p(offs), G,
+                                  ctypes.c_void_p(qr), ctypes.c_void_p(sr), ctypes.c_void_p(qc),
+                                  ctypes.c_void_p(sc), None)
+
+
+def test_dual_rejections(L):
+    assert _dual(L, M=100) == mxq.EBADSHAPE
+    assert _dual(L, N=96) == mxq.EBADSHAPE
+    assert _dual(L, M=-128) == mxq.EBADSHAPE
+    assert _dual(L, M=1 << 31) == mxq.EBADSHAPE
+    assert _dual(L, offs=None, G=1) == mxq.EBADOFFS          # NULL offs needs G == 0
+    assert _dual(L, offs=A + (1 << 30), G=0) == mxq.EBADOFFS  # offs needs G >= 1
+    assert _dual(L, offs=A + (1 << 30), G=mxq.MAX_GROUPS + 1) == mxq.EBADOFFS
+    assert _dual(L, offs=A + (1 << 30) + 2, G=4) == mxq.EALIGN
+    assert _dual(L, x=0) == mxq.ENULL
+    assert _dual(L, sc=0) == mxq.ENULL
+    assert _dual(L, x=A + 8) == mxq.EALIGN
+    assert _dual(L, qc=A + 8 * 128 * 128 + 4) == mxq.EALIGN
+    assert _dual(L, qr=A + 128 * 128) == mxq.EOVERLAP         # q_row inside x
+    assert _dual(L, sr=A + 8 * 128 * 128 + 16) == mxq.EOVERLAP  # s_row inside q_col
+    assert _dual(L, offs=A + 64, G=4) == mxq.EOVERLAP           # offs inside x
+    # empty problems are no-ops that touch nothing (NULL pointers allowed)
+    assert L.mxq_quantize_2d_dual(None, 0, 128, None, 0, None, None, None, None, None) == mxq.OK
+    assert L.mxq_quantize_2d_dual(None, 128, 0, None, 0, None, None, None, None, None) == mxq.OK
+
+
+def _pack(L, x=A, dtype=0, rows=4, cols=16, q=A + 4096, e=A + 8192, p=A + 12288):
+    return L.mx9_pack(ctypes.c_void_p(x), dtype, rows, cols, ctypes.c_void_p(q),
+                      ctypes.c_void_p(e), ctypes.c_void_p(p), None)
+
+
+def _unpack(L, q=A, e=A + 4096, p=A + 8192, y=A + 12288, dtype=0, rows=4, cols=16):
+    return L.mx9_unpack(ctypes.c_void_p(q), ctypes.c_void_p(e), ctypes.c_void_p(p),
+                        ctypes.c_void_p(y), dtype, rows, cols, None)
+
+
+def test_mx9_rejections(L):
+    assert _pack(L, dtype=2) == mxq.EBADDTYPE
+    assert _pack(L, cols=15) == mxq.EBADSHAPE
+    assert _pack(L, rows=-1) == mxq.EBADSHAPE
+    assert _pack(L, x=0) == mxq.ENULL
+    assert _pack(L, x=A + 4) == mxq.EALIGN
+    assert _pack(L, q=A + 16) == mxq.EOVERLAP  # q inside x (x spans 256 bytes)
+    assert _pack(L, e=A + 4096 + 32) == mxq.EOVERLAP
+    assert _pack(L, rows=0) == mxq.OK
+    assert _unpack(L, dtype=7) == mxq.EBADDTYPE
+    assert _unpack(L, cols=8) == mxq.EBADSHAPE
+    assert _unpack(L, y=0) == mxq.ENULL
+    assert _unpack(L, y=A + 12288 + 8) == mxq.EALIGN
+    assert _unpack(L, y=A + 16) == mxq.EOVERLAP
+    assert _unpack(L, cols=0) == mxq.OK
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros((128, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mxq.quantize_2d_dual(x)
+    with pytest.raises(ValueError):
+        mxq.mx9_pack(torch.zeros((4, 16)))
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_fails_loudly(L):
+    """With no GPU the first CUDA call fails and the library reports it (no CPU fallback)."""
+    assert _dual(L) == mxq.ECUDA
+    assert _pack(L) == mxq.ECUDA
