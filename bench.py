@@ -1,0 +1,547 @@
+"""Benchmark of the MX block-quantization hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. mxq_quantize_2d_dual on the MoE-grouped bf16 [65536, 7168] tensor
+     (64 K-groups, offs[-1] = 57344, 8192-row uncovered tail);
+  2. mx9_pack of an fp32 [16384, 8192] N(0,1) tensor;
+  3. mx9_unpack of its packed parts back to fp32.
+Throughput = algorithmic bytes of the step (4.0625 B per element for the dual
+cast; 5.125 B per element for each MX9 pass on fp32) / device time.  Inputs
+are larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on the
+host cores instead, on bounded samples of the same workload.  `--sweep` prints
+one extra line per throughput-sweep shape, timed under CUDA-graph replay.
+
+Multi-GPU (torchrun): every rank quantizes its own tensors (independent work,
+no collective on the data path); the timing is the max over ranks and `value`
+aggregates all ranks' bytes (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dual-axis MXFP8 quantize HBM GB/s (% of GB300 peak); MX9 pack/unpack GB/s"
+DUAL_M, DUAL_N = 65536, 7168
+MX9_ROWS, MX9_COLS = 16384, 8192
+B_DUAL = 4.0625          # bytes per element: 2 in + 1 + 1 + 1/32 + 1/32 out
+B_MX9_F32 = 5.125        # bytes per element: 4 (fp32) + 1 (q) + 1/16 + 1/16
+WORKLOAD = (f"MoE-grouped dual-axis MXFP8 bf16[{DUAL_M},{DUAL_N}] 64 groups offs[-1]=57344 "
+            f"+ MX9 pack/unpack fp32[{MX9_ROWS},{MX9_COLS}]")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mxq_dual_moe_65536x7168.md")
+
+
+def step_bytes() -> dict:
+    return {"mxq_dual": B_DUAL * DUAL_M * DUAL_N,
+            "mx9_pack": B_MX9_F32 * MX9_ROWS * MX9_COLS,
+            "mx9_unpack": B_MX9_F32 * MX9_ROWS * MX9_COLS}
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("mxq_dual.cu", "mxq_device.cuh"):
+        with open(os.path.join(ROOT, "mx_block_quantization_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dual kernel from the committed ncu summary,
+    or None when there is none or the kernel source changed since."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mxq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        try:
+            rows = open(self.path).read().strip().splitlines()
+        except OSError:
+            rows = []
+        for row in rows:
+            parts = [p.strip() for p in row.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_init():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank moved bytes_per_step per step; the job
+    took the slowest rank's time (weak scaling)."""
+    return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings (the reference arm and the cpu_baseline key)
+# ---------------------------------------------------------------------------
+def oracle_sample_inputs(rank_seed: int):
+    """Host inputs for the oracle samples: the full workloads' generators, cut
+    to windows (tiles and 16-element blocks are independent)."""
+    from mx_block_quantization_gb300 import workloads as W
+    xd = W.normal_bf16((1024, DUAL_N), seed=rank_seed, scale=0.02)   # first rows of the MoE tensor
+    offs = W.moe_group_offsets(seed=rank_seed + 1)
+    offs_win = np.minimum(offs, 1024).astype(np.int32)                # groups clipped to the window
+    xm = W.normal_f32((512, MX9_COLS), seed=rank_seed)
+    return xd, offs_win, xm
+
+
+def time_oracle(budget_s: float, rank_seed: int = 0) -> dict:
+    """Run the oracle over repeated samples for about budget_s; GB/s of algorithmic bytes."""
+    import oracle
+    xd, offs, xm = oracle_sample_inputs(rank_seed)
+    done_bytes, t0 = 0.0, time.perf_counter()
+    reps = 0
+    while True:
+        oracle.mxfp8_dual(xd, offs)
+        q, e, p = oracle.mx9_pack(xm)
+        oracle.mx9_unpack(q, e, p, "f32", *xm.shape)
+        done_bytes += B_DUAL * xd.size + 2 * B_MX9_F32 * xm.size
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{reps} x (dual bf16[1024,{DUAL_N}] window of the MoE tensor with its "
+                       f"groups clipped + MX9 pack/unpack fp32[512,{MX9_COLS}]), single thread, "
+                       f"{dt:.1f} s")}
+
+
+def run_reference(args):
+    # rank 0 alone times the oracle; other ranks exit without work
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    if rank != 0:
+        return 0
+    import oracle
+    from mx_block_quantization_gb300 import workloads as W
+    oracle.build()
+    # each step: one 128x1024 tile-row window of the MoE tensor + MX9 on fp32[8, 8192]
+    xd = W.normal_bf16((128, 1024), seed=0, scale=0.02)
+    offs = np.array([128], np.int32)
+    xm = W.normal_f32((8, MX9_COLS), seed=0)
+    step_b = B_DUAL * xd.size + 2 * B_MX9_F32 * xm.size
+
+    def one():
+        oracle.mxfp8_dual(xd, offs)
+        q, e, p = oracle.mx9_pack(xm)
+        oracle.mx9_unpack(q, e, p, "f32", *xm.shape)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    gbs = step_b * args.steps / dt / 1e9
+    sample = (f"per step: dual bf16[128,1024] window of the MoE tensor + MX9 pack/unpack "
+              f"fp32[8,{MX9_COLS}], single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+
+    import mx_block_quantization_gb300 as mxq
+    from mx_block_quantization_gb300 import workloads as W
+    from mx_block_quantization_gb300.build import build_library
+
+    rank, world, local = dist_init()
+    build_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    seed = rank  # each rank quantizes its own tensors
+
+    # ---- inputs (host-generated, seeded) and outputs, resident in HBM
+    xd_h, offs_h = W.moe_grouped(seed=seed)
+    xm_h = W.normal_f32((MX9_ROWS, MX9_COLS), seed=seed)
+    x = torch.from_numpy(xd_h.view(np.int16)).view(torch.bfloat16).to(dev)
+    offs = torch.from_numpy(offs_h).to(dev)
+    xm = torch.from_numpy(xm_h).to(dev)
+    kw = dict(dtype=torch.uint8, device=dev)
+    M, N = DUAL_M, DUAL_N
+    dual_out = mxq.DualOutputs(torch.empty((M, N), **kw), torch.empty((M * N // 32,), **kw),
+                               torch.empty((N, M), **kw), torch.empty((M * N // 32,), **kw))
+    nb = MX9_ROWS * MX9_COLS // 16
+    q = torch.empty((nb, 16), dtype=torch.int8, device=dev)
+    e = torch.empty((nb,), dtype=torch.uint8, device=dev)
+    p = torch.empty((nb, 1), dtype=torch.uint8, device=dev)
+    y = torch.empty((MX9_ROWS, MX9_COLS), dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mxq.quantize_2d_dual(x, offs, out=dual_out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mxq.mx9_pack(xm, out=(q, e, p), stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        mxq.mx9_unpack(q, e, p, torch.float32, (MX9_ROWS, MX9_COLS), out=y, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert mxq.device_status(clear=True) == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    assert mxq.device_status(clear=True) == 0
+
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    value = aggregate_gbs(sum(step_bytes().values()), args.steps, world, total_ms)
+    per = {"mxq_dual": [], "mx9_pack": [], "mx9_unpack": []}
+    for ev in evs:
+        per["mxq_dual"].append(ev[0].elapsed_time(ev[1]))
+        per["mx9_pack"].append(ev[1].elapsed_time(ev[2]))
+        per["mx9_unpack"].append(ev[2].elapsed_time(ev[3]))
+    sb = step_bytes()
+    bytes_per_step = sum(sb.values())
+    ms_per_step = total_ms / args.steps
+    peak, peak_kind = measured_peak()
+    breakdown = {}
+    for k, v in per.items():
+        avg = float(np.mean(v))
+        gbs = sb[k] / (avg / 1e3) / 1e9
+        breakdown[k] = {"avg_us": avg * 1e3, "gbs": gbs, "frac_of_measured": gbs / peak,
+                        "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                        "algorithmic_bytes": sb[k]}
+    dual_avg_s = float(np.mean(per["mxq_dual"])) / 1e3
+    achieved = sb["mxq_dual"] / dual_avg_s / 1e9
+    traffic = profiled_traffic()
+    roofline = {"bound": "hbm", "kernel": "mxq_dual_kernel", "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "algorithmic_bytes": sb["mxq_dual"]}
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, mxq, torch, dev, stream, xd_h, offs, xm_h, dual_out, (q, e, p), y, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 (129 MB); no flush",
+                           "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 3 * args.steps, "clocks": clocks, "breakdown": breakdown}
+        print(json.dumps(line), flush=True)
+    if args.sweep:
+        run_sweep(mxq, torch, dev, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, mxq, torch, dev, stream, xd_h, offs, xm_h, dual_out, mx9_parts, y, world):
+    """Same step through the public API with pinned host buffers: H2D of the
+    inputs, the three calls, D2H of every output, all inside the timed region."""
+    x_h = torch.from_numpy(xd_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    xm_hp = torch.from_numpy(xm_h).pin_memory()
+    x_d = torch.empty_like(x_h, device=dev)
+    xm_d = torch.empty_like(xm_hp, device=dev)
+    outs_d = list(dual_out) + list(mx9_parts) + [y]
+    outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs_d]
+    q, e, p = mx9_parts
+
+    def one():
+        x_d.copy_(x_h, non_blocking=True)
+        xm_d.copy_(xm_hp, non_blocking=True)
+        mxq.quantize_2d_dual(x_d, offs, out=dual_out, stream=stream)
+        mxq.mx9_pack(xm_d, out=(q, e, p), stream=stream)
+        mxq.mx9_unpack(q, e, p, torch.float32, tuple(xm_d.shape), out=y, stream=stream)
+        for h, d in zip(outs_h, outs_d):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    steps = args.e2e_steps
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    h2d = x_h.numel() * 2 + xm_hp.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    return {"value": aggregate_gbs(sum(step_bytes().values()), steps, world, ms), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+def run_sweep(mxq, torch, dev, rank):
+    """Throughput sweep shapes under CUDA-graph replay (20 launches per graph)."""
+    from mx_block_quantization_gb300 import workloads as W
+    peak, kind = measured_peak()
+    for (M, N) in W.SWEEP_SHAPES:
+        res = {}
+        x = torch.from_numpy(W.normal_bf16((M, N), seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+        kw = dict(dtype=torch.uint8, device=dev)
+        out = mxq.DualOutputs(torch.empty((M, N), **kw), torch.empty((M * N // 32,), **kw),
+                              torch.empty((N, M), **kw), torch.empty((M * N // 32,), **kw))
+        res["mxq_dual"] = (graph_time(torch, dev, lambda s: mxq.quantize_2d_dual(x, out=out, stream=s)),
+                           B_DUAL * M * N)
+        del x, out
+        for dt, tdt, bpe in (("f32", torch.float32, B_MX9_F32), ("bf16", torch.bfloat16, 3.125)):
+            xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
+            q, e, p = mxq.mx9_pack(xm)
+            yy = torch.empty_like(xm)
+            res[f"mx9_pack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx9_pack(xm, out=(q, e, p), stream=s)),
+                                     bpe * M * N)
+            res[f"mx9_unpack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx9_unpack(
+                q, e, p, tdt, (M, N), out=yy, stream=s)), bpe * M * N)
+            del xm, q, e, p, yy
+        if rank == 0:
+            line = {"sweep_shape": [M, N], "peak_gbs": peak, "peak_kind": kind,
+                    "l2_resident": (B_DUAL * M * N) < 129e6}
+            for k, (us, b) in res.items():
+                gbs = b / (us / 1e6) / 1e9
+                line[k] = {"us": us, "gbs": gbs, "frac_of_measured": gbs / peak,
+                           "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+
+
+def graph_time(torch, dev, launch, per_graph=20, replays=10):
+    """Median per-launch time (us) of `launch` captured per_graph times into one
+    CUDA graph; the graph must contain kernel work (timed replay > 0)."""
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        launch(s)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(per_graph):
+            launch(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(replays):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        a.record(cur)
+        g.replay()
+        b.record(cur)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b) * 1e3 / per_graph)
+    med = statistics.median(times)
+    assert med > 0.5, "graph replay took no time: nothing was captured"
+    return med
+
+
+def run_case(args):
+    """Launch one kernel `--warmup` times on one shape (for profiler captures)."""
+    import torch
+
+    import mx_block_quantization_gb300 as mxq
+    from mx_block_quantization_gb300 import workloads as W
+    from mx_block_quantization_gb300.build import build_library
+
+    build_library()
+    M, N = (int(v) for v in args.shape.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    if args.case == "dual":
+        offs = None
+        if args.groups:
+            offs = torch.from_numpy(W.moe_group_offsets(args.groups, M // 128 - M // 1024)).to(dev)
+        x = torch.from_numpy(W.normal_bf16((M, N), seed=0, scale=0.02).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        for _ in range(args.warmup):
+            mxq.quantize_2d_dual(x, offs)
+    else:
+        tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
+        xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
+        q, e, p = mxq.mx9_pack(xm)
+        for _ in range(args.warmup):
+            if args.case.startswith("pack"):
+                mxq.mx9_pack(xm, out=(q, e, p))
+            else:
+                mxq.mx9_unpack(q, e, p, tdt, (M, N))
+    torch.cuda.synchronize()
+    assert mxq.device_status(clear=True) == 0
+    print(json.dumps({"case": args.case, "shape": [M, N], "launches": args.warmup}))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also print one line per throughput-sweep shape (graph replay)")
+    ap.add_argument("--case", choices=["dual", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16"],
+                    help="only launch this kernel --warmup times on --shape (profiling)")
+    ap.add_argument("--shape", default="16384x7168")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="with --case dual: that many K-groups and a 1/8 uncovered tail")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.case:
+        return run_case(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -7,8 +7,8 @@
 // (set when the pair's exponent is below E); scale exponent
 // k = max(E - 6 - prime, -126); q = clamp(round_half_even(x / 2^k), -127, 127).
 //
-// Both kernels are streaming and HBM-bound: a grid sized to the SM count
-// walks 16-byte chunks with four independent chunks in flight per thread;
+// Both kernels are streaming and HBM-bound: one full wave of resident blocks
+// walks 16-byte chunks with several independent chunks in flight per thread;
 // groups of neighbouring lanes that share a block (4 lanes for fp32 data, 2
 // for bf16 data) combine exponents and prime bits with shuffles, so every
 // load and store of a warp covers contiguous bytes.
@@ -23,8 +23,20 @@ namespace {
 
 using namespace mxq;
 
+// Launch shape.  The defaults are the measured best on GB300; the macros only
+// exist so that other shapes can be built for measurement.
+#ifndef MXQ_MX9_UNROLL
+#define MXQ_MX9_UNROLL 4
+#endif
+#ifndef MXQ_MX9_UNPACK_UNROLL
+#define MXQ_MX9_UNPACK_UNROLL 4
+#endif
+#ifndef MXQ_MX9_PACK_MINBLOCKS
+#define MXQ_MX9_PACK_MINBLOCKS 4
+#endif
 constexpr int kBlock = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = MXQ_MX9_UNROLL;              // pack: 16-byte input chunks in flight
+constexpr int kUnrollUnpack = MXQ_MX9_UNPACK_UNROLL;  // unpack: chunks per thread per iteration
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
@@ -54,7 +66,7 @@ __device__ __forceinline__ uint32_t quant_elem(float x, int k) {
 // ---------------------------------------------------------------------------
 // pack, fp32 input: 4 lanes per 16-element block, 4 elements per lane
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBlock) mx9_pack_f32_kernel(const uint4* __restrict__ x,
+__global__ void __launch_bounds__(kBlock, MXQ_MX9_PACK_MINBLOCKS) mx9_pack_f32_kernel(const uint4* __restrict__ x,
                                                               int64_t nchunks,
                                                               uint32_t* __restrict__ q,
                                                               uint8_t* __restrict__ max_exp,
@@ -103,7 +115,7 @@ __global__ void __launch_bounds__(kBlock) mx9_pack_f32_kernel(const uint4* __res
 // ---------------------------------------------------------------------------
 // pack, bf16 input: 2 lanes per block, 8 elements per lane
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBlock) mx9_pack_bf16_kernel(const uint4* __restrict__ x,
+__global__ void __launch_bounds__(kBlock, MXQ_MX9_PACK_MINBLOCKS) mx9_pack_bf16_kernel(const uint4* __restrict__ x,
                                                                int64_t nchunks,
                                                                uint2* __restrict__ q,
                                                                uint8_t* __restrict__ max_exp,
@@ -166,10 +178,10 @@ __global__ void __launch_bounds__(kBlock) mx9_unpack_kernel(const uint32_t* __re
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kBlock + (threadIdx.x - lane);
-  for (int64_t base = warp0; base < nchunks; base += stride * kUnroll) {
-    uint32_t qv[kUnroll], ev[kUnroll], pv[kUnroll];
+  for (int64_t base = warp0; base < nchunks; base += stride * kUnrollUnpack) {
+    uint32_t qv[kUnrollUnpack], ev[kUnrollUnpack], pv[kUnrollUnpack];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kUnrollUnpack; ++u) {
       const int64_t c = base + u * stride + lane;
       if (c < nchunks) {
         qv[u] = __ldcs(q + c);
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(kBlock) mx9_unpack_kernel(const uint32_t* __re
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kUnrollUnpack; ++u) {
       const int64_t c = base + u * stride + lane;
       if (c >= nchunks) continue;
       const int E = static_cast<int>(ev[u]) - 127;
@@ -204,9 +216,16 @@ __global__ void __launch_bounds__(kBlock) mx9_unpack_kernel(const uint32_t* __re
   }
 }
 
-unsigned grid_for(int64_t nchunks, int sms) {
+// One full wave: as many resident blocks as the kernel's occupancy allows on
+// every SM, or fewer when the problem is small.
+template <typename Kernel>
+unsigned grid_for(Kernel kernel, int64_t nchunks, int sms) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
   const int64_t want = (nchunks + kBlock - 1) / kBlock;
-  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kBlock);
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<unsigned>(want < cap ? want : cap);
 }
 
@@ -244,12 +263,12 @@ extern "C" int mx9_pack(const void* x, int dtype, int64_t rows, int64_t cols, in
   cudaError_t e;
   if (dtype == MXQ_F32) {
     const int64_t nchunks = n / 4;
-    cfg.gridDim = dim3(grid_for(nchunks, sms));
+    cfg.gridDim = dim3(grid_for(mx9_pack_f32_kernel, nchunks, sms));
     e = cudaLaunchKernelEx(&cfg, mx9_pack_f32_kernel, static_cast<const uint4*>(x), nchunks,
                            reinterpret_cast<uint32_t*>(q), max_exp, prime);
   } else {
     const int64_t nchunks = n / 8;
-    cfg.gridDim = dim3(grid_for(nchunks, sms));
+    cfg.gridDim = dim3(grid_for(mx9_pack_bf16_kernel, nchunks, sms));
     e = cudaLaunchKernelEx(&cfg, mx9_pack_bf16_kernel, static_cast<const uint4*>(x), nchunks,
                            reinterpret_cast<uint2*>(q), max_exp, prime);
   }
@@ -277,7 +296,8 @@ extern "C" int mx9_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
 
   const int64_t nchunks = n / 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid_for(nchunks, sms));
+  cfg.gridDim = dim3(dtype == MXQ_F32 ? grid_for(mx9_unpack_kernel<false>, nchunks, sms)
+                                      : grid_for(mx9_unpack_kernel<true>, nchunks, sms));
   cfg.blockDim = dim3(kBlock);
   cfg.stream = stream;
   const uint32_t* q32 = reinterpret_cast<const uint32_t*>(q);

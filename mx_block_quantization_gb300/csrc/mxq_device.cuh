@@ -207,8 +207,18 @@ __device__ __forceinline__ uint32_t e8m0_rceil_from_bits(uint32_t a, uint32_t in
 
 // The reciprocal multiplier 2^(127 - s) as an fp32: normal for s <= 253, the
 // subnormal 2^-127 for s = 254 (used only by Inf-carrying colwise blocks).
+// For s = 255 (the NaN rule) it is a NaN, so every product is NaN and every
+// byte of the block casts to the E4M3 NaN 0x7F without a separate override.
 __device__ __forceinline__ float e8m0_multiplier(uint32_t s) {
-  return __uint_as_float(s >= 254u ? 0x00400000u : (254u - s) << 23);
+  return __uint_as_float(s == 255u ? 0x7FFFFFFFu : s == 254u ? 0x00400000u : (254u - s) << 23);
+}
+
+// Per-half max(|a|, |b|) of two bf16x2 words, NaN-propagating (the sign bit of
+// the result is the xor of the inputs' signs and is masked off by the caller).
+__device__ __forceinline__ uint32_t bf16x2_absmax_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // IEEE single multiply, round to nearest, subnormals kept (no flush).

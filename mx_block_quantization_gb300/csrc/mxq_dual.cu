@@ -10,7 +10,7 @@
 // GB300 design (a persistent, warp-specialized, bandwidth-bound kernel; no
 // tensor cores because there is no contraction):
 //   * one CTA per SM walks 128x128 tiles t = blockIdx.x + k * gridDim.x;
-//   * warp 16 (producer) streams tiles into a 4-stage shared-memory ring with
+//   * warp 16 (producer) streams tiles into a 3-stage shared-memory ring with
 //     2-D TMA loads (two 64-column boxes per tile, 128-byte swizzle);
 //   * warps 0..15 (consumers) run the rowwise and the colwise pass of a tile
 //     from shared memory and write its four outputs into a double-buffered
@@ -36,9 +36,23 @@ namespace {
 
 using namespace mxq;
 
+// Pipeline shape.  The defaults are the measured best on GB300; the macros
+// only exist so that other shapes can be built for measurement.
+#ifndef MXQ_DUAL_STAGES
+#define MXQ_DUAL_STAGES 3
+#endif
+#ifndef MXQ_DUAL_OUTBUFS
+#define MXQ_DUAL_OUTBUFS 2
+#endif
+#ifndef MXQ_DUAL_GROUP_ROWS
+#define MXQ_DUAL_GROUP_ROWS 8
+#endif
 constexpr int kTile = 128;
-constexpr int kStages = 4;
-constexpr int kConsumerWarps = 16;
+constexpr int kStages = MXQ_DUAL_STAGES;              // input ring depth (tiles)
+constexpr int kOutBufs = MXQ_DUAL_OUTBUFS;            // staged output tiles
+constexpr int kRowWarps = 8;                          // rowwise consumers
+constexpr int kConsumerWarps = 2 * kRowWarps;         // + as many colwise consumers
+constexpr int kGroupRows = MXQ_DUAL_GROUP_ROWS;       // tile rows per rasterization group
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kStoreWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;  // 576
@@ -52,13 +66,13 @@ constexpr uint32_t kAtomBytes = 512;                   // one 128x4 scale atom
 // buffer starts on a 1024-byte boundary as the 128-byte swizzle requires).
 constexpr uint32_t kOffIn = 0;
 constexpr uint32_t kOffQRow = kOffIn + kStages * kInStageBytes;
-constexpr uint32_t kOffQCol = kOffQRow + 2 * kQTileBytes;
-constexpr uint32_t kOffSRow = kOffQCol + 2 * kQTileBytes;
-constexpr uint32_t kOffSCol = kOffSRow + 2 * kAtomBytes;
-constexpr uint32_t kOffZero = kOffSCol + 2 * kAtomBytes;
+constexpr uint32_t kOffQCol = kOffQRow + kOutBufs * kQTileBytes;
+constexpr uint32_t kOffSRow = kOffQCol + kOutBufs * kQTileBytes;
+constexpr uint32_t kOffSCol = kOffSRow + kOutBufs * kAtomBytes;
+constexpr uint32_t kOffZero = kOffSCol + kOutBufs * kAtomBytes;
 constexpr uint32_t kOffOffs = kOffZero + kAtomBytes;
 constexpr uint32_t kOffBar = kOffOffs + 4 * MXQ_MAX_GROUPS;
-constexpr uint32_t kNumBars = 2 * kStages + 4;
+constexpr uint32_t kNumBars = 2 * kStages + 2 * kOutBufs;
 constexpr uint32_t kOffFlag = kOffBar + 8 * kNumBars;
 constexpr uint32_t kSmemUsed = kOffFlag + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
@@ -73,7 +87,7 @@ struct Bars {
   __device__ uint32_t full(int s) const { return base + 8u * s; }
   __device__ uint32_t empty(int s) const { return base + 8u * (kStages + s); }
   __device__ uint32_t ofull(int b) const { return base + 8u * (2 * kStages + b); }
-  __device__ uint32_t oempty(int b) const { return base + 8u * (2 * kStages + 2 + b); }
+  __device__ uint32_t oempty(int b) const { return base + 8u * (2 * kStages + kOutBufs + b); }
 };
 
 // Physical byte offset of 16-byte chunk `chunk` of row `row` in a buffer of
@@ -82,40 +96,20 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// ---------------------------------------------------------------------------
-// Rowwise pass: thread (r, j) quantizes the 1x32 block j of tile row r.
-// Warp w owns rows 8w..8w+7; lane l takes row 8w + l/4 and block l%4.
-// Block j lives in half-tile j/2, logical chunks (j%2)*4 .. +3.  Lanes with
-// j >= 2 read their four chunks rotated by two so that each 8-lane phase of
-// the 128-bit loads touches eight distinct bank groups; the rotation swaps
-// which 16-byte half of the output each half of the registers feeds.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void rowwise_pass(uint32_t in_s, uint32_t qrow_s, uint32_t srow_s,
-                                             int warp, int lane) {
-  const int r = warp * 8 + (lane >> 2);
-  const int j = lane & 3;
-  const int rot = (j >> 1) * 2;
-  const uint32_t half = in_s + static_cast<uint32_t>(j >> 1) * kHalfBytes;
-
-  uint32_t w[16];
+// Amax of a run of bf16x2 words as sign-masked bf16 bits (per half): one
+// NaN-propagating abs-max per word, then the sign bits cleared once.
+template <int kWords>
+__device__ __forceinline__ uint32_t absmax_bits(const uint32_t* w) {
+  uint32_t m = w[0];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int chunk = (j & 1) * 4 + ((k + rot) & 3);
-    const uint4 v = lds128(half + swz(r, chunk));
-    w[4 * k + 0] = v.x;
-    w[4 * k + 1] = v.y;
-    w[4 * k + 2] = v.z;
-    w[4 * k + 3] = v.w;
-  }
+  for (int i = 1; i < kWords; ++i) m = bf16x2_absmax_nan(m, w[i]);
+  return m & 0x7FFF7FFFu;
+}
 
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-  const uint32_t amax = max(m & 0xFFFFu, m >> 16);
-  const uint32_t s = e8m0_rceil_from_bits(amax, 255u);
-  const float mult = e8m0_multiplier(s);
-
-  uint32_t o[8];
+// Cast one 1x32 row block (16 bf16x2 words, element order) with the
+// multiplier of its scale and pack the E4M3 bytes in element order, four per
+// output word.
+__device__ __forceinline__ void cast_row_block(const uint32_t* w, float mult, uint32_t* o) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t a = w[2 * i], b = w[2 * i + 1];
@@ -123,59 +117,77 @@ __device__ __forceinline__ void rowwise_pass(uint32_t in_s, uint32_t qrow_s, uin
                                    fmul_rn_noftz(bf16_lo_f32(a), mult));
     const uint32_t hi = cvt_e4m3x2(fmul_rn_noftz(bf16_hi_f32(b), mult),
                                    fmul_rn_noftz(bf16_lo_f32(b), mult));
-    o[i] = (s == 255u) ? 0x7F7F7F7Fu : (lo | (hi << 16));
+    o[i] = lo | (hi << 16);
   }
-  // registers o[0..3] hold block bytes (rot ? 16..31 : 0..15), o[4..7] the rest
-  const int first = 2 * j + (rot ? 1 : 0);
-  const int second = 2 * j + (rot ? 0 : 1);
-  sts128(qrow_s + swz(r, first), o[0], o[1], o[2], o[3]);
-  sts128(qrow_s + swz(r, second), o[4], o[5], o[6], o[7]);
-  // scale (r, j) of this tile's 128x4 atom
-  sts8(srow_s + static_cast<uint32_t>((r & 31) * 16 + (r >> 5) * 4 + j), s);
 }
 
 // ---------------------------------------------------------------------------
-// Colwise pass: warp w takes row block i = w/4 (rows 32i..32i+31) and the 32
-// columns 32*(w%4)..+31; lane l takes column pair p = 16*(w%4) + l%16
-// (columns 2p, 2p+1) over rows 32i + 16*(l/16) .. +15.  The two 16-row halves
-// combine their amax with one shuffle.  Lanes of the upper half visit their
-// rows with the 4-row groups swapped (row index j ^ 4) so that the two halves
-// of each 32-bit load hit different bank groups; the swap is undone when the
-// output words are placed.  E4M3 bytes for four consecutive rows of one
-// column are packed into one word, so each lane emits two 16-byte runs of
-// q_col (one per column), written with the swizzle into the [n][m] tile.
+// Rowwise warps (0..7): lane l of warp w takes tile row r = 16w + l/2 and the
+// half-tile h = l%2, i.e. the two 1x32 blocks 2h and 2h+1.  Lanes with h = 1
+// visit their eight 16-byte chunks in the order k ^ 4, so the 128-bit loads
+// and stores of every 8-lane phase hit eight distinct bank groups; that only
+// changes which block (jA, jB) each half of the registers belongs to.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void rowwise_pass(uint32_t in_s, uint32_t qrow_s, uint32_t srow_s,
+                                             int warp, int lane) {
+  const int r = 16 * warp + (lane >> 1);
+  const int h = lane & 1;
+  const uint32_t half = in_s + static_cast<uint32_t>(h) * kHalfBytes;
+  uint32_t w[32];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = lds128(half + swz(r, k ^ (4 * h)));
+    w[4 * k + 0] = v.x;
+    w[4 * k + 1] = v.y;
+    w[4 * k + 2] = v.z;
+    w[4 * k + 3] = v.w;
+  }
+  const int jA = 3 * h, jB = 2 * h + 1 - h;  // block of registers 0..15 / 16..31
+  const uint32_t mA = absmax_bits<16>(w), mB = absmax_bits<16>(w + 16);
+  const uint32_t sA = e8m0_rceil_from_bits(max(mA & 0xFFFFu, mA >> 16), 255u);
+  const uint32_t sB = e8m0_rceil_from_bits(max(mB & 0xFFFFu, mB >> 16), 255u);
+  uint32_t oA[8], oB[8];
+  cast_row_block(w, e8m0_multiplier(sA), oA);
+  cast_row_block(w + 16, e8m0_multiplier(sB), oB);
+  sts128(qrow_s + swz(r, 2 * jA), oA[0], oA[1], oA[2], oA[3]);
+  sts128(qrow_s + swz(r, 2 * jA + 1), oA[4], oA[5], oA[6], oA[7]);
+  sts128(qrow_s + swz(r, 2 * jB), oB[0], oB[1], oB[2], oB[3]);
+  sts128(qrow_s + swz(r, 2 * jB + 1), oB[4], oB[5], oB[6], oB[7]);
+  const uint32_t at = static_cast<uint32_t>((r & 31) * 16 + (r >> 5) * 4);
+  sts8(srow_s + at + jA, sA);
+  sts8(srow_s + at + jB, sB);
+}
+
+// ---------------------------------------------------------------------------
+// Colwise warps (8..15): warp 8 + w' takes row block i = w'/2 (rows 32i..+31)
+// and lane l one column pair p (columns 2p, 2p+1) down all 32 rows.  Lanes
+// 0..15 take pairs 16q + l of half-tile 0 and lanes 16..31 pairs
+// 32 + 16(1-q) + (l-16) of half-tile 1 (q = w' % 2), so the two half-warps of
+// every 32-bit load read different bank groups of the same row.  E4M3 bytes
+// of four consecutive rows of one column form one word: each lane emits 32
+// contiguous bytes of q_col per column.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void colwise_pass(uint32_t in_s, uint32_t qcol_s, uint32_t scol_s,
-                                             int warp, int lane) {
-  const int i = warp >> 2;
-  const int cg = warp & 3;
-  const int pl = lane & 15;
-  const int rh = lane >> 4;
-  const int p = cg * 16 + pl;
-  const uint32_t half = in_s + static_cast<uint32_t>(cg >> 1) * kHalfBytes;
-  const int chunk = (p & 31) >> 2;
-  const uint32_t within = static_cast<uint32_t>(p & 3) * 4u;
-
-  uint32_t w[16];
+                                             int cwarp, int lane) {
+  const int i = cwarp >> 1;
+  const int q = cwarp & 1;
+  const int p = lane < 16 ? 16 * q + lane : 32 + 16 * (1 - q) + (lane - 16);
+  const uint32_t half = in_s + (p >= 32 ? kHalfBytes : 0u);
+  const int pp = p & 31;
+  const int chunk = pp >> 2;
+  const uint32_t within = static_cast<uint32_t>(pp & 3) * 4u;
+  uint32_t w[32];
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    const int row = 32 * i + 16 * rh + (jj ^ (4 * rh));
-    w[jj] = lds32(half + swz(row, chunk) + within);
-  }
+  for (int j = 0; j < 32; ++j) w[j] = lds32(half + swz(32 * i + j, chunk) + within);
 
-  uint32_t m = 0;
-#pragma unroll
-  for (int jj = 0; jj < 16; ++jj) m = __vmaxu2(m, w[jj] & 0x7FFF7FFFu);
-  m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+  const uint32_t m = absmax_bits<32>(w);
   const uint32_t s_lo = e8m0_rceil_from_bits(m & 0xFFFFu, 254u);  // column 2p
   const uint32_t s_hi = e8m0_rceil_from_bits(m >> 16, 254u);      // column 2p+1
   const float mult_lo = e8m0_multiplier(s_lo);
   const float mult_hi = e8m0_multiplier(s_hi);
-
-  // c_lo[g] / c_hi[g]: rows 4g..4g+3 (register order) of column 2p / 2p+1
-  uint32_t c_lo[4], c_hi[4];
+  uint32_t L[8], H[8];
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < 8; ++g) {
     const uint32_t a = w[4 * g], b = w[4 * g + 1], c = w[4 * g + 2], d = w[4 * g + 3];
     const uint32_t l01 = cvt_e4m3x2(fmul_rn_noftz(bf16_lo_f32(b), mult_lo),
                                     fmul_rn_noftz(bf16_lo_f32(a), mult_lo));
@@ -185,31 +197,31 @@ __device__ __forceinline__ void colwise_pass(uint32_t in_s, uint32_t qcol_s, uin
                                     fmul_rn_noftz(bf16_hi_f32(a), mult_hi));
     const uint32_t h23 = cvt_e4m3x2(fmul_rn_noftz(bf16_hi_f32(d), mult_hi),
                                     fmul_rn_noftz(bf16_hi_f32(c), mult_hi));
-    c_lo[g] = (s_lo == 255u) ? 0x7F7F7F7Fu : (l01 | (l23 << 16));
-    c_hi[g] = (s_hi == 255u) ? 0x7F7F7F7Fu : (h01 | (h23 << 16));
+    L[g] = l01 | (l23 << 16);
+    H[g] = h01 | (h23 << 16);
   }
-  // undo the 4-row-group swap of the upper half: output group G is c[G ^ rh]
-  const bool sw = rh != 0;
-  const uint32_t L0 = sw ? c_lo[1] : c_lo[0], L1 = sw ? c_lo[0] : c_lo[1];
-  const uint32_t L2 = sw ? c_lo[3] : c_lo[2], L3 = sw ? c_lo[2] : c_lo[3];
-  const uint32_t H0 = sw ? c_hi[1] : c_hi[0], H1 = sw ? c_hi[0] : c_hi[1];
-  const uint32_t H2 = sw ? c_hi[3] : c_hi[2], H3 = sw ? c_hi[2] : c_hi[3];
-
   const int n_lo = 2 * p, n_hi = 2 * p + 1;  // tile-local columns = q_col tile rows
-  const int mchunk = 2 * i + rh;             // 16-byte run of rows within the 128
-  const uint32_t a_lo = qcol_s + swz(n_lo, mchunk);
-  const uint32_t a_hi = qcol_s + swz(n_hi, mchunk);
-  if ((pl & 7) < 4) {
-    sts128(a_lo, L0, L1, L2, L3);
-    sts128(a_hi, H0, H1, H2, H3);
-  } else {
-    sts128(a_hi, H0, H1, H2, H3);
-    sts128(a_lo, L0, L1, L2, L3);
-  }
-  if (rh == 0) {
-    sts8(scol_s + static_cast<uint32_t>((n_lo & 31) * 16 + (n_lo >> 5) * 4 + i), s_lo);
-    sts8(scol_s + static_cast<uint32_t>((n_hi & 31) * 16 + (n_hi >> 5) * 4 + i), s_hi);
-  }
+  sts128(qcol_s + swz(n_lo, 2 * i), L[0], L[1], L[2], L[3]);
+  sts128(qcol_s + swz(n_lo, 2 * i + 1), L[4], L[5], L[6], L[7]);
+  sts128(qcol_s + swz(n_hi, 2 * i), H[0], H[1], H[2], H[3]);
+  sts128(qcol_s + swz(n_hi, 2 * i + 1), H[4], H[5], H[6], H[7]);
+  sts8(scol_s + static_cast<uint32_t>((n_lo & 31) * 16 + (n_lo >> 5) * 4 + i), s_lo);
+  sts8(scol_s + static_cast<uint32_t>((n_hi & 31) * 16 + (n_hi >> 5) * 4 + i), s_hi);
+}
+
+// Tile t of the persistent walk -> (tile row, tile column).  Tiles go in
+// groups of kGroupRows tile rows, column by column inside a group, so the
+// tiles in flight at one time cover a compact block: x rows and q_row rows
+// are read/written in runs of several tiles, and so are the rows of the
+// transposed q_col.
+__device__ __forceinline__ void tile_coords(int64_t t, int64_t TM, int64_t TN, int64_t* ti,
+                                            int64_t* tj) {
+  const int64_t per_group = static_cast<int64_t>(kGroupRows) * TN;
+  const int64_t g = t / per_group;
+  const int64_t local = t - g * per_group;
+  const int64_t rows = min(static_cast<int64_t>(kGroupRows), TM - g * kGroupRows);
+  *ti = g * kGroupRows + local % rows;
+  *tj = local / rows;
 }
 
 // First g with offs[g] > row (the group holding `row`), by binary search.
@@ -240,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int64_t TN = N / kTile;
-  const int64_t T = static_cast<int64_t>(M / kTile) * TN;
+  const int64_t TM = M / kTile;
+  const int64_t T = TM * TN;
   const int64_t my_tiles =
       (static_cast<int64_t>(blockIdx.x) < T) ? (T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), kConsumerWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kOutBufs; ++b) {
       mbar_init(bars.ofull(b), kConsumerWarps);
       mbar_init(bars.oempty(b), 1);
     }
@@ -270,13 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t issued = 0;
   const bool is_producer = (warp == kProducerWarp) && (lane == 0);
   auto issue_load = [&](int64_t k) {
-    const int64_t t = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
-    const int32_t ti = static_cast<int32_t>(t / TN), tj = static_cast<int32_t>(t % TN);
+    int64_t ti, tj;
+    tile_coords(blockIdx.x + k * static_cast<int64_t>(gridDim.x), TM, TN, &ti, &tj);
     const int s = static_cast<int>(k % kStages);
     const uint32_t dst = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
     mbar_arrive_expect_tx(bars.full(s), kInStageBytes);
-    tma_load_2d(dst, &tm_x, tj * kTile, ti * kTile, bars.full(s));
-    tma_load_2d(dst + kHalfBytes, &tm_x, tj * kTile + 64, ti * kTile, bars.full(s));
+    const int32_t c0 = static_cast<int32_t>(tj * kTile), r0 = static_cast<int32_t>(ti * kTile);
+    tma_load_2d(dst, &tm_x, c0, r0, bars.full(s));
+    tma_load_2d(dst + kHalfBytes, &tm_x, c0 + 64, r0, bars.full(s));
   };
   auto drain_loads = [&]() {
     for (int64_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
@@ -313,20 +327,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- consumers
     for (int64_t k = 0; k < my_tiles; ++k) {
       const int s = static_cast<int>(k % kStages);
-      const int b = static_cast<int>(k & 1);
+      const int b = static_cast<int>(k % kOutBufs);
       // every lane waits (acquiring the barrier's data); the warp leaves
       // together if any lane gave up, so no warp-collective runs short
       bool ok = mbar_wait_bounded(bars.full(s), static_cast<uint32_t>((k / kStages) & 1),
                                   abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT);
-      if (ok && k >= 2)
-        ok = mbar_wait_bounded(bars.oempty(b), static_cast<uint32_t>(((k >> 1) - 1) & 1),
+      if (ok && k >= kOutBufs)
+        ok = mbar_wait_bounded(bars.oempty(b), static_cast<uint32_t>(((k / kOutBufs) - 1) & 1),
                                abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       const uint32_t in_s = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
-      rowwise_pass(in_s, base + kOffQRow + b * kQTileBytes, base + kOffSRow + b * kAtomBytes, warp,
-                   lane);
-      colwise_pass(in_s, base + kOffQCol + b * kQTileBytes, base + kOffSCol + b * kAtomBytes, warp,
-                   lane);
+      if (warp < kRowWarps)
+        rowwise_pass(in_s, base + kOffQRow + b * kQTileBytes, base + kOffSRow + b * kAtomBytes,
+                     warp, lane);
+      else
+        colwise_pass(in_s, base + kOffQCol + b * kQTileBytes, base + kOffSCol + b * kAtomBytes,
+                     warp - kRowWarps, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.empty(s));
       fence_proxy_async_smem();
@@ -354,12 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_qcol);
       const int64_t Mrows = M;
       for (int64_t k = 0; k < my_tiles; ++k) {
-        const int b = static_cast<int>(k & 1);
-        if (!mbar_wait_bounded(bars.ofull(b), static_cast<uint32_t>((k >> 1) & 1), abort_flag,
+        const int b = static_cast<int>(k % kOutBufs);
+        if (!mbar_wait_bounded(bars.ofull(b), static_cast<uint32_t>((k / kOutBufs) & 1), abort_flag,
                                &g_mxq_status, MXQ_DEV_TIMEOUT))
           break;
-        const int64_t t = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
-        const int64_t ti = t / TN, tj = t % TN;
+        int64_t ti, tj;
+        tile_coords(blockIdx.x + k * static_cast<int64_t>(gridDim.x), TM, TN, &ti, &tj);
         const int64_t row0 = ti * kTile;
         tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
                      base + kOffQRow + b * kQTileBytes);

@@ -1,0 +1,68 @@
+"""The multi-process path of bench.py on CPU (gloo, world size 2): the timing
+reduction takes the slowest rank, the aggregate counts every rank's bytes, and
+under torchrun only rank 0 prints the reference line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    bench.barrier(world)
+    got = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+    out.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 15.0, 1: 15.0}
+
+
+def test_weak_scaling_aggregate():
+    sys.path.insert(0, ROOT)
+    import bench
+    one = bench.aggregate_gbs(1e9, 10, 1, 1000.0)
+    two = bench.aggregate_gbs(1e9, 10, 2, 1000.0)
+    assert one == pytest.approx(10.0) and two == pytest.approx(20.0)
+    assert bench.aggregate_gbs(1e9, 10, 2, 2000.0) == pytest.approx(10.0)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
