@@ -7,11 +7,13 @@
 // (set when the pair's exponent is below E); scale exponent
 // k = max(E - 6 - prime, -126); q = clamp(round_half_even(x / 2^k), -127, 127).
 //
-// Both kernels are streaming and HBM-bound: one full wave of resident blocks
-// walks 16-byte chunks with several independent chunks in flight per thread;
-// groups of neighbouring lanes that share a block (4 lanes for fp32 data, 2
-// for bf16 data) combine exponents and prime bits with shuffles, so every
-// load and store of a warp covers contiguous bytes.
+// pack: persistent and warp-specialized like the dual-axis kernel.  One
+// producer warp streams contiguous runs of blocks into a shared-memory
+// ring with 1-D bulk copies (TMA); each consumer thread then owns one whole
+// 16-element block, so exponents and prime bits need no shuffles, and writes
+// its 16 q bytes, exponent byte and prime byte with coalesced stores.
+// unpack: a streaming kernel, one wave of resident blocks, 4 lanes per block,
+// exact q * 2^k built without conversion instructions.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,159 +27,221 @@ using namespace mxq;
 
 // Launch shape.  The defaults are the measured best on GB300; the macros only
 // exist so that other shapes can be built for measurement.
-#ifndef MXQ_MX9_UNROLL
-#define MXQ_MX9_UNROLL 4
+#ifndef MXQ_MX9_PACK_F32_WARPS
+#define MXQ_MX9_PACK_F32_WARPS 8
+#endif
+#ifndef MXQ_MX9_PACK_F32_RING_KB
+#define MXQ_MX9_PACK_F32_RING_KB 64
+#endif
+#ifndef MXQ_MX9_PACK_BF16_WARPS
+#define MXQ_MX9_PACK_BF16_WARPS 12
+#endif
+#ifndef MXQ_MX9_PACK_BF16_RING_KB
+#define MXQ_MX9_PACK_BF16_RING_KB 96
+#endif
+#ifndef MXQ_MX9_PACK_CTAS_PER_SM
+#define MXQ_MX9_PACK_CTAS_PER_SM 2
 #endif
 #ifndef MXQ_MX9_UNPACK_UNROLL
 #define MXQ_MX9_UNPACK_UNROLL 4
 #endif
-#ifndef MXQ_MX9_PACK_MINBLOCKS
-#define MXQ_MX9_PACK_MINBLOCKS 4
-#endif
-constexpr int kBlock = 256;
-constexpr int kUnroll = MXQ_MX9_UNROLL;              // pack: 16-byte input chunks in flight
-constexpr int kUnrollUnpack = MXQ_MX9_UNPACK_UNROLL;  // unpack: chunks per thread per iteration
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+constexpr int kUnpackBlock = 256;
+constexpr int kUnrollUnpack = MXQ_MX9_UNPACK_UNROLL;
+
+// Sticky status word of this file's kernels (MXQ_DEV_* bits).
+__device__ unsigned int g_mx9_status = 0;
+
+// Pack kernel shape per input type: consumer warps (one 16-element block per
+// consumer thread and stage), one producer warp, a ring of stages.
+template <bool kBF16>
+struct PackShape {
+  static constexpr int kWarps = kBF16 ? MXQ_MX9_PACK_BF16_WARPS : MXQ_MX9_PACK_F32_WARPS;
+  static constexpr int kThreads = (kWarps + 1) * 32;
+  static constexpr int kBlocksPerStage = kWarps * 32;
+  static constexpr uint32_t kBlockBytes = kBF16 ? 32u : 64u;  // 16 elements
+  static constexpr uint32_t kStageBytes = kBlocksPerStage * kBlockBytes;
+  static constexpr uint32_t kRingBytes =
+      (kBF16 ? MXQ_MX9_PACK_BF16_RING_KB : MXQ_MX9_PACK_F32_RING_KB) * 1024u;
+  static constexpr int kStages = static_cast<int>(kRingBytes / kStageBytes);
+  static constexpr uint32_t kOffBar = kStages * kStageBytes;
+  static constexpr uint32_t kOffFlag = kOffBar + 16u * kStages;
+  static constexpr uint32_t kSmemBytes = kOffFlag + 16u + 128u;  // + alignment slack
+  static_assert(kStages >= 2, "ring too small");
+  static_assert(kSmemBytes <= 227u * 1024u, "shared memory budget");
+};
+
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
+
+// Multiplier 2^-k of a pair from the block's exponent field eb8 (E = eb8 - 127)
+// and the pair's prime bit t: k = max(E - 6 - t, -126), 127 - k = min(260 - eb8 + t, 253).
+__device__ __forceinline__ float pair_multiplier(uint32_t eb8, uint32_t t) {
+  return __uint_as_float(min(260u - eb8 + t, 253u) << 23);
+}
+
+// x * 2^-k (exact multiply, no flush) rounded half-to-even to an integer and
+// clamped to [-127, 127]; cvt.rni gives 0 for NaN and saturates +-Inf.
+__device__ __forceinline__ uint32_t q_byte(float x, float mult) {
+  const int r = __float2int_rn(fmul_rn_noftz(x, mult));
+  return static_cast<uint32_t>(max(-127, min(127, r))) & 0xFFu;
+}
+
+// One block of 16 elements given as 16 fp32 bit patterns.
+__device__ __forceinline__ void pack_block(const uint32_t* f, uint4* q, uint32_t* eb_out,
+                                           uint32_t* prime_out) {
+  uint32_t pe[8];
+  uint32_t eb = 0;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    pe[p] = max(f[2 * p] & 0x7F800000u, f[2 * p + 1] & 0x7F800000u);
+    eb = max(eb, pe[p]);
+  }
+  const uint32_t eb8 = eb >> 23;
+  uint32_t bits = 0, word[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t t = pe[p] < eb;
+    bits |= t << p;
+    const float m = pair_multiplier(eb8, t);
+    const uint32_t two = q_byte(__uint_as_float(f[2 * p]), m) |
+                         (q_byte(__uint_as_float(f[2 * p + 1]), m) << 8);
+    word[p >> 1] |= two << (16 * (p & 1));
+  }
+  *q = make_uint4(word[0], word[1], word[2], word[3]);
+  *eb_out = eb8;
+  *prime_out = bits;
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(PackShape<kBF16>::kThreads, MXQ_MX9_PACK_CTAS_PER_SM)
+    mx9_pack_kernel(const uint8_t* __restrict__ x, int64_t nb, uint4* __restrict__ q,
+                    uint8_t* __restrict__ max_exp, uint8_t* __restrict__ prime) {
+  using S = PackShape<kBF16>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + S::kOffFlag);
+  auto full = [&](int s) { return base + S::kOffBar + 8u * s; };
+  auto empty = [&](int s) { return base + S::kOffBar + 8u * (S::kStages + s); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t nchunks = (nb + S::kBlocksPerStage - 1) / S::kBlocksPerStage;
+  const int64_t my =
+      static_cast<int64_t>(blockIdx.x) < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), S::kWarps);
+    }
+    *abort_flag = 0u;
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == S::kWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    int64_t issued = 0;
+    for (int64_t i = 0; i < my; ++i) {
+      const int s = static_cast<int>(i % S::kStages);
+      if (i >= S::kStages &&
+          !mbar_wait_bounded(empty(s), static_cast<uint32_t>(((i / S::kStages) - 1) & 1),
+                             abort_flag, &g_mx9_status, MXQ_DEV_TIMEOUT))
+        break;
+      const int64_t b0 = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * S::kBlocksPerStage;
+      const int64_t nblk = nb - b0 < S::kBlocksPerStage ? nb - b0 : S::kBlocksPerStage;
+      const uint32_t bytes = static_cast<uint32_t>(nblk) * S::kBlockBytes;
+      mbar_arrive_expect_tx(full(s), bytes);
+      bulk_load_1d(base + static_cast<uint32_t>(s) * S::kStageBytes, x + b0 * S::kBlockBytes,
+                   bytes, full(s));
+      issued = i + 1;
+    }
+    // drain (a no-op after a normal run: consumers waited for every stage)
+    for (int64_t i = issued > S::kStages ? issued - S::kStages : 0; i < issued; ++i)
+      mbar_wait_drain(full(static_cast<int>(i % S::kStages)),
+                      static_cast<uint32_t>((i / S::kStages) & 1));
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  for (int64_t i = 0; i < my; ++i) {
+    const int s = static_cast<int>(i % S::kStages);
+    const bool ok = mbar_wait_bounded(full(s), static_cast<uint32_t>((i / S::kStages) & 1),
+                                      abort_flag, &g_mx9_status, MXQ_DEV_TIMEOUT);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return;
+    const int64_t blk = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * S::kBlocksPerStage + tid;
+    if (blk < nb) {
+      const uint32_t src = base + static_cast<uint32_t>(s) * S::kStageBytes + tid * S::kBlockBytes;
+      uint32_t f[16];
+      if (kBF16) {
+        const uint4 a = lds128(src), b = lds128(src + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          f[2 * k] = w[k] << 16;             // exact widening of each bf16
+          f[2 * k + 1] = w[k] & 0xFFFF0000u;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 a = lds128(src + 16u * k);
+          f[4 * k] = a.x;
+          f[4 * k + 1] = a.y;
+          f[4 * k + 2] = a.z;
+          f[4 * k + 3] = a.w;
+        }
+      }
+      uint4 qv;
+      uint32_t eb8, bits;
+      pack_block(f, &qv, &eb8, &bits);
+      __stcs(q + blk, qv);
+      max_exp[blk] = static_cast<uint8_t>(eb8);
+      prime[blk] = static_cast<uint8_t>(bits);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// unpack
+// ---------------------------------------------------------------------------
 
 // 2^e as fp32 for e in the normal range [-126, 127].
 __device__ __forceinline__ float exp2_normal(int e) {
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
-// round_half_even(v) clamped to [-127, 127]; NaN -> 0, +-Inf -> +-127.
-__device__ __forceinline__ uint32_t q_byte(float v) {
-  int r = __float2int_rn(v);  // cvt.rni.s32.f32: ties to even, NaN -> 0, saturating
-  r = max(-127, min(127, r));
-  return static_cast<uint32_t>(r) & 0xFFu;
+__device__ __forceinline__ float fadd_rn_noftz(float a, float b) {
+  float r;
+  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
-// x / 2^k as an exact multiply by 2^-k (k in [-126, 122] makes 2^-k normal).
-__device__ __forceinline__ uint32_t quant_elem(float x, int k) {
-  return q_byte(fmul_rn_noftz(x, exp2_normal(-k)));
+// Exact float of a small integer q (|q| < 2^22) without a conversion
+// instruction: the bits of 1.5 * 2^23 + q, minus 1.5 * 2^23.
+__device__ __forceinline__ float small_int_to_float(int32_t q) {
+  return fadd_rn_noftz(__int_as_float(0x4B400000 + q), -12582912.0f);
 }
 
-// ---------------------------------------------------------------------------
-// pack, fp32 input: 4 lanes per 16-element block, 4 elements per lane
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBlock, MXQ_MX9_PACK_MINBLOCKS) mx9_pack_f32_kernel(const uint4* __restrict__ x,
-                                                              int64_t nchunks,
-                                                              uint32_t* __restrict__ q,
-                                                              uint8_t* __restrict__ max_exp,
-                                                              uint8_t* __restrict__ prime) {
-  const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kBlock + (threadIdx.x - lane);
-  for (int64_t base = warp0; base < nchunks; base += stride * kUnroll) {
-    uint4 v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * stride + lane;
-      v[u] = c < nchunks ? ldg_stream(x + c) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * stride + lane;
-      const uint32_t b0 = (v[u].x >> 23) & 0xFF, b1 = (v[u].y >> 23) & 0xFF;
-      const uint32_t b2 = (v[u].z >> 23) & 0xFF, b3 = (v[u].w >> 23) & 0xFF;
-      const uint32_t p0 = max(b0, b1), p1 = max(b2, b3);
-      uint32_t eb = max(p0, p1);
-      eb = max(eb, __shfl_xor_sync(0xFFFFFFFFu, eb, 1));
-      eb = max(eb, __shfl_xor_sync(0xFFFFFFFFu, eb, 2));  // biased E of the block
-      const uint32_t t0 = p0 < eb, t1 = p1 < eb;
-      const int E = static_cast<int>(eb) - 127;
-      const int k0 = max(E - 6 - static_cast<int>(t0), -126);
-      const int k1 = max(E - 6 - static_cast<int>(t1), -126);
-      const uint32_t word = quant_elem(__uint_as_float(v[u].x), k0) |
-                            (quant_elem(__uint_as_float(v[u].y), k0) << 8) |
-                            (quant_elem(__uint_as_float(v[u].z), k1) << 16) |
-                            (quant_elem(__uint_as_float(v[u].w), k1) << 24);
-      uint32_t bits = (t0 | (t1 << 1)) << (2 * (lane & 3));
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
-      if (c < nchunks) {
-        __stcs(q + c, word);
-        if ((lane & 3) == 0) {
-          max_exp[c >> 2] = static_cast<uint8_t>(eb);
-          prime[c >> 2] = static_cast<uint8_t>(bits);
-        }
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// pack, bf16 input: 2 lanes per block, 8 elements per lane
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBlock, MXQ_MX9_PACK_MINBLOCKS) mx9_pack_bf16_kernel(const uint4* __restrict__ x,
-                                                               int64_t nchunks,
-                                                               uint2* __restrict__ q,
-                                                               uint8_t* __restrict__ max_exp,
-                                                               uint8_t* __restrict__ prime) {
-  const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kBlock + (threadIdx.x - lane);
-  for (int64_t base = warp0; base < nchunks; base += stride * kUnroll) {
-    uint4 v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * stride + lane;
-      v[u] = c < nchunks ? ldg_stream(x + c) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * stride + lane;
-      const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t pe[4];  // biased exponent of each pair (one word = one pair)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pe[i] = max((wd[i] >> 7) & 0xFF, (wd[i] >> 23) & 0xFF);
-      uint32_t eb = max(max(pe[0], pe[1]), max(pe[2], pe[3]));
-      eb = max(eb, __shfl_xor_sync(0xFFFFFFFFu, eb, 1));
-      const int E = static_cast<int>(eb) - 127;
-      uint32_t tb = 0, lo = 0, hi = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t t = pe[i] < eb;
-        tb |= t << i;
-        const int k = max(E - 6 - static_cast<int>(t), -126);
-        const uint32_t pair = quant_elem(bf16_lo_f32(wd[i]), k) |
-                              (quant_elem(bf16_hi_f32(wd[i]), k) << 8);
-        if (i < 2)
-          lo |= pair << (16 * i);
-        else
-          hi |= pair << (16 * (i - 2));
-      }
-      uint32_t bits = tb << (4 * (lane & 1));
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
-      if (c < nchunks) {
-        __stcs(q + c, make_uint2(lo, hi));
-        if ((lane & 1) == 0) {
-          max_exp[c >> 1] = static_cast<uint8_t>(eb);
-          prime[c >> 1] = static_cast<uint8_t>(bits);
-        }
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// unpack: 4 lanes per block, 4 elements per lane; fp32 or bf16 output
-// ---------------------------------------------------------------------------
+// 4 lanes per block, 4 elements per lane; q * 2^k is exact (|q| <= 127,
+// k >= -126) except for overflow in max_exp 255 blocks.
 template <bool kBF16>
-__global__ void __launch_bounds__(kBlock) mx9_unpack_kernel(const uint32_t* __restrict__ q,
-                                                            const uint8_t* __restrict__ max_exp,
-                                                            const uint8_t* __restrict__ prime,
-                                                            void* __restrict__ y,
-                                                            int64_t nchunks) {
+__global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
+    const uint32_t* __restrict__ q, const uint8_t* __restrict__ max_exp,
+    const uint8_t* __restrict__ prime, void* __restrict__ y, int64_t nchunks) {
   const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kBlock + (threadIdx.x - lane);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kUnpackBlock;
+  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kUnpackBlock + (threadIdx.x - lane);
   for (int64_t base = warp0; base < nchunks; base += stride * kUnrollUnpack) {
     uint32_t qv[kUnrollUnpack], ev[kUnrollUnpack], pv[kUnrollUnpack];
 #pragma unroll
@@ -199,13 +263,13 @@ __global__ void __launch_bounds__(kBlock) mx9_unpack_kernel(const uint32_t* __re
       const int pbits = static_cast<int>(pv[u] >> (2 * (lane & 3)));
       const float s0 = exp2_normal(max(E - 6 - (pbits & 1), -126));
       const float s1 = exp2_normal(max(E - 6 - ((pbits >> 1) & 1), -126));
-      const float y0 = static_cast<float>(static_cast<int8_t>(qv[u] & 0xFF)) * s0;
-      const float y1 = static_cast<float>(static_cast<int8_t>((qv[u] >> 8) & 0xFF)) * s0;
-      const float y2 = static_cast<float>(static_cast<int8_t>((qv[u] >> 16) & 0xFF)) * s1;
-      const float y3 = static_cast<float>(static_cast<int8_t>(qv[u] >> 24)) * s1;
+      const int32_t w = static_cast<int32_t>(qv[u]);
+      const float y0 = fmul_rn_noftz(small_int_to_float((w << 24) >> 24), s0);
+      const float y1 = fmul_rn_noftz(small_int_to_float((w << 16) >> 24), s0);
+      const float y2 = fmul_rn_noftz(small_int_to_float((w << 8) >> 24), s1);
+      const float y3 = fmul_rn_noftz(small_int_to_float(w >> 24), s1);
       if (kBF16) {
-        // q * 2^k has at most 7 significant bits: the top half of the fp32 is
-        // the exact bf16 (Inf included)
+        // at most 7 significant bits: the top half of the fp32 is the exact bf16
         const uint32_t lo = (__float_as_uint(y0) >> 16) | (__float_as_uint(y1) & 0xFFFF0000u);
         const uint32_t hi = (__float_as_uint(y2) >> 16) | (__float_as_uint(y3) & 0xFFFF0000u);
         __stcs(reinterpret_cast<uint2*>(y) + c, make_uint2(lo, hi));
@@ -219,12 +283,13 @@ __global__ void __launch_bounds__(kBlock) mx9_unpack_kernel(const uint32_t* __re
 // One full wave: as many resident blocks as the kernel's occupancy allows on
 // every SM, or fewer when the problem is small.
 template <typename Kernel>
-unsigned grid_for(Kernel kernel, int64_t nchunks, int sms) {
+unsigned unpack_grid(Kernel kernel, int64_t nchunks, int sms) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kUnpackBlock, 0) !=
+          cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int64_t want = (nchunks + kBlock - 1) / kBlock;
+  const int64_t want = (nchunks + kUnpackBlock - 1) / kUnpackBlock;
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<unsigned>(want < cap ? want : cap);
 }
@@ -236,7 +301,42 @@ int check_dims(int dtype, int64_t rows, int64_t cols) {
   return MXQ_OK;
 }
 
+template <bool kBF16>
+cudaError_t launch_pack(const void* x, int64_t nb, int8_t* q, uint8_t* max_exp, uint8_t* prime,
+                        int sms, int dev, cudaStream_t stream) {
+  using S = PackShape<kBF16>;
+  static bool attr_done[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {  // benign race: setting the same attribute twice is harmless
+    const cudaError_t e = cudaFuncSetAttribute(
+        mx9_pack_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int64_t nchunks = (nb + S::kBlocksPerStage - 1) / S::kBlocksPerStage;
+  const int64_t cap = static_cast<int64_t>(sms) * MXQ_MX9_PACK_CTAS_PER_SM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nchunks < cap ? nchunks : cap));
+  cfg.blockDim = dim3(S::kThreads);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, mx9_pack_kernel<kBF16>, static_cast<const uint8_t*>(x), nb,
+                            reinterpret_cast<uint4*>(q), max_exp, prime);
+}
+
 }  // namespace
+
+namespace mxq {
+// Read (and optionally clear) this file's status word; used by mxq_device_status.
+int mx9_status_read(unsigned int* out, bool clear) {
+  if (cudaMemcpyFromSymbol(out, g_mx9_status, sizeof *out) != cudaSuccess) return MXQ_ECUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_mx9_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ECUDA;
+  }
+  return MXQ_OK;
+}
+}  // namespace mxq
 
 extern "C" int mx9_pack(const void* x, int dtype, int64_t rows, int64_t cols, int8_t* q,
                         uint8_t* max_exp, uint8_t* prime, cudaStream_t stream) {
@@ -254,24 +354,12 @@ extern "C" int mx9_pack(const void* x, int dtype, int64_t rows, int64_t cols, in
       {reinterpret_cast<uintptr_t>(prime), static_cast<uint64_t>(n / 16)},
   };
   if (ranges_overlap(r, 4)) return MXQ_EOVERLAP;
-  const int sms = sm_count_current_device(nullptr);
+  int dev = 0;
+  const int sms = sm_count_current_device(&dev);
   if (sms <= 0) return MXQ_ECUDA;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kBlock);
-  cfg.stream = stream;
-  cudaError_t e;
-  if (dtype == MXQ_F32) {
-    const int64_t nchunks = n / 4;
-    cfg.gridDim = dim3(grid_for(mx9_pack_f32_kernel, nchunks, sms));
-    e = cudaLaunchKernelEx(&cfg, mx9_pack_f32_kernel, static_cast<const uint4*>(x), nchunks,
-                           reinterpret_cast<uint32_t*>(q), max_exp, prime);
-  } else {
-    const int64_t nchunks = n / 8;
-    cfg.gridDim = dim3(grid_for(mx9_pack_bf16_kernel, nchunks, sms));
-    e = cudaLaunchKernelEx(&cfg, mx9_pack_bf16_kernel, static_cast<const uint4*>(x), nchunks,
-                           reinterpret_cast<uint2*>(q), max_exp, prime);
-  }
+  const cudaError_t e = dtype == MXQ_F32
+                            ? launch_pack<false>(x, n / 16, q, max_exp, prime, sms, dev, stream)
+                            : launch_pack<true>(x, n / 16, q, max_exp, prime, sms, dev, stream);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 
@@ -296,9 +384,9 @@ extern "C" int mx9_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
 
   const int64_t nchunks = n / 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(dtype == MXQ_F32 ? grid_for(mx9_unpack_kernel<false>, nchunks, sms)
-                                      : grid_for(mx9_unpack_kernel<true>, nchunks, sms));
-  cfg.blockDim = dim3(kBlock);
+  cfg.gridDim = dim3(dtype == MXQ_F32 ? unpack_grid(mx9_unpack_kernel<false>, nchunks, sms)
+                                      : unpack_grid(mx9_unpack_kernel<true>, nchunks, sms));
+  cfg.blockDim = dim3(kUnpackBlock);
   cfg.stream = stream;
   const uint32_t* q32 = reinterpret_cast<const uint32_t*>(q);
   const cudaError_t e =

@@ -499,14 +499,21 @@ extern "C" int mxq_quantize_2d_dual(const void* x, int64_t M, int64_t N, const i
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 
+namespace mxq {
+int mx9_status_read(unsigned int* out, bool clear);  // mx9.cu
+}
+
+// The device status word is the OR of the per-file words of the kernels.
 extern "C" int mxq_device_status(uint32_t* out, int clear) {
   if (!out) return MXQ_ENULL;
-  unsigned int v = 0;
+  unsigned int v = 0, w = 0;
   if (cudaMemcpyFromSymbol(&v, g_mxq_status, sizeof v) != cudaSuccess) return MXQ_ECUDA;
   if (clear) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_mxq_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ECUDA;
   }
-  *out = v;
+  const int rc = mxq::mx9_status_read(&w, clear != 0);
+  if (rc != MXQ_OK) return rc;
+  *out = v | w;
   return MXQ_OK;
 }
