@@ -133,6 +133,41 @@ int mx9_unpack(const int8_t *q, const uint8_t *max_exp, const uint8_t *prime, vo
                int64_t rows, int64_t cols, cudaStream_t stream);
 
 /*
+ * The three-pass composition that the fused cast replaces ([AO] description,
+ * first paragraph: a 1x32 cast along N, a 32x1 cast along M and a standalone
+ * K-groups swizzle of the colwise scales, reading x twice).  Kept so that the
+ * fused kernel can be measured against it and for callers that want one axis.
+ *
+ * mxq_quantize_1x32: q_row and s_row exactly as mxq_quantize_2d_dual writes
+ *   them.  Arguments as there.
+ * mxq_quantize_32x1: q_col as mxq_quantize_2d_dual writes it, and the colwise
+ *   scales as a plain row-major [N, M/32] matrix s_rm (byte n*(M/32) + i for
+ *   the 32x1 block of rows 32i..32i+31 of column n).  Its block rule is the
+ *   separate 32x1 cast's ([AO] description, NaN paragraph): the amax skips NaN
+ *   (an all-NaN block takes scale 0), +-Inf gives scale 254 and +-448 data,
+ *   a NaN element stays a NaN byte.  So it differs from the fused cast only in
+ *   blocks that hold NaN.
+ * mxq_swizzle_kgroups: s_rm [N, M/32] -> s_col in the fused cast's layout:
+ *   per-group blocked slabs, zeros from N*offs[G-1]/32 on (offs/G as for
+ *   mxq_quantize_2d_dual; invalid offs are detected on the device, nothing is
+ *   written and MXQ_DEV_BADOFFS is set).
+ * mxq_quantize_2d_dual_3pass: the three launches in order on `stream`, with
+ *   the caller's `workspace` (>= N*M/32 bytes, 16-byte aligned, not
+ *   overlapping any other buffer; returns MXQ_EBADSHAPE if too small) holding
+ *   s_rm between the second and third.
+ * All pointers are device pointers; 16-byte alignment as for the fused cast.
+ */
+int mxq_quantize_1x32(const void *x, int64_t M, int64_t N, uint8_t *q_row, uint8_t *s_row,
+                      cudaStream_t stream);
+int mxq_quantize_32x1(const void *x, int64_t M, int64_t N, uint8_t *q_col, uint8_t *s_rm,
+                      cudaStream_t stream);
+int mxq_swizzle_kgroups(const uint8_t *s_rm, int64_t N, int64_t M, const int32_t *offs, int32_t G,
+                        uint8_t *s_col, cudaStream_t stream);
+int mxq_quantize_2d_dual_3pass(const void *x, int64_t M, int64_t N, const int32_t *offs, int32_t G,
+                               uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                               uint8_t *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Device status word of the current device: a sticky OR of MXQ_DEV_* bits set
  * by kernels since the last clear.  Writes it to *out and clears it when
  * `clear` is non-zero.  This call synchronizes the device (it reads device

@@ -67,6 +67,14 @@ def lib() -> ctypes.CDLL:
         L.mx9_pack.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
         L.mx9_unpack.restype = ctypes.c_int
         L.mx9_unpack.argtypes = [vp, vp, vp, vp, ctypes.c_int, i64, i64, vp]
+        L.mxq_quantize_1x32.restype = ctypes.c_int
+        L.mxq_quantize_1x32.argtypes = [vp, i64, i64, vp, vp, vp]
+        L.mxq_quantize_32x1.restype = ctypes.c_int
+        L.mxq_quantize_32x1.argtypes = [vp, i64, i64, vp, vp, vp]
+        L.mxq_swizzle_kgroups.restype = ctypes.c_int
+        L.mxq_swizzle_kgroups.argtypes = [vp, i64, i64, vp, i32, vp, vp]
+        L.mxq_quantize_2d_dual_3pass.restype = ctypes.c_int
+        L.mxq_quantize_2d_dual_3pass.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp, i64, vp]
         L.mxq_device_status.restype = ctypes.c_int
         L.mxq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.mxq_status_string.restype = ctypes.c_char_p
@@ -161,6 +169,122 @@ def quantize_2d_dual(x, offs=None, *, out: Optional[DualOutputs] = None, stream=
             *(ctypes.c_void_p(t.data_ptr()) for t in out), _stream_handle(x.device, stream))
     if rc != OK:
         raise MxqError(rc, "mxq_quantize_2d_dual")
+    return out
+
+
+def _check_x_offs(x, offs):
+    torch = _torch()
+    _check_cuda(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    G = 0
+    if offs is not None:
+        _check_cuda(offs, "offs")
+        if offs.dtype != torch.int32 or offs.dim() != 1 or offs.device != x.device:
+            raise ValueError("offs must be a 1-D int32 tensor on x's device")
+        G = offs.numel()
+    return G
+
+
+def _u8(t, n, name, device):
+    torch = _torch()
+    _check_cuda(t, name)
+    if t.dtype != torch.uint8 or t.numel() != n or t.device != device:
+        raise ValueError(f"{name} must be a uint8 tensor of {n} elements on x's device")
+
+
+def quantize_1x32(x, *, out=None, stream=None):
+    """Rowwise-only cast: (q_row [M, N], s_row [M*N/32] blocked), as quantize_2d_dual."""
+    torch = _torch()
+    _check_x_offs(x, None)
+    M, N = x.shape
+    kw = dict(dtype=torch.uint8, device=x.device)
+    q_row, s_row = out if out is not None else (torch.empty((M, N), **kw),
+                                                torch.empty((M * N // 32,), **kw))
+    _u8(q_row, M * N, "q_row", x.device)
+    _u8(s_row, M * N // 32, "s_row", x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().mxq_quantize_1x32(ctypes.c_void_p(x.data_ptr()), M, N,
+                                     ctypes.c_void_p(q_row.data_ptr()),
+                                     ctypes.c_void_p(s_row.data_ptr()),
+                                     _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_quantize_1x32")
+    return q_row, s_row
+
+
+def quantize_32x1(x, *, out=None, stream=None):
+    """Colwise-only cast with the separate 32x1 cast's NaN rule: (q_col [N, M],
+    s_rm [N, M/32] row-major scales)."""
+    torch = _torch()
+    _check_x_offs(x, None)
+    M, N = x.shape
+    kw = dict(dtype=torch.uint8, device=x.device)
+    q_col, s_rm = out if out is not None else (torch.empty((N, M), **kw),
+                                               torch.empty((N, M // 32), **kw))
+    _u8(q_col, M * N, "q_col", x.device)
+    _u8(s_rm, M * N // 32, "s_rm", x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().mxq_quantize_32x1(ctypes.c_void_p(x.data_ptr()), M, N,
+                                     ctypes.c_void_p(q_col.data_ptr()),
+                                     ctypes.c_void_p(s_rm.data_ptr()),
+                                     _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_quantize_32x1")
+    return q_col, s_rm
+
+
+def swizzle_kgroups(s_rm, offs=None, *, out=None, stream=None):
+    """Row-major colwise scales [N, M/32] -> the fused cast's grouped blocked s_col."""
+    torch = _torch()
+    _check_cuda(s_rm, "s_rm")
+    if s_rm.dtype != torch.uint8 or s_rm.dim() != 2:
+        raise ValueError("s_rm must be a 2-D uint8 tensor [N, M/32]")
+    N, C = s_rm.shape
+    M = 32 * C
+    G = 0
+    if offs is not None:
+        _check_cuda(offs, "offs")
+        if offs.dtype != torch.int32 or offs.dim() != 1 or offs.device != s_rm.device:
+            raise ValueError("offs must be a 1-D int32 tensor on s_rm's device")
+        G = offs.numel()
+    if out is None:
+        out = torch.empty((N * M // 32,), dtype=torch.uint8, device=s_rm.device)
+    _u8(out, N * M // 32, "s_col", s_rm.device)
+    with torch.cuda.device(s_rm.device):
+        rc = lib().mxq_swizzle_kgroups(ctypes.c_void_p(s_rm.data_ptr()), N, M,
+                                       ctypes.c_void_p(offs.data_ptr() if offs is not None else 0),
+                                       G, ctypes.c_void_p(out.data_ptr()),
+                                       _stream_handle(s_rm.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_swizzle_kgroups")
+    return out
+
+
+def quantize_2d_dual_3pass(x, offs=None, *, workspace=None, out=None, stream=None) -> DualOutputs:
+    """The three-pass composition (1x32, 32x1, swizzle) with a caller workspace of
+    >= M*N/32 bytes (allocated here when not given)."""
+    torch = _torch()
+    G = _check_x_offs(x, offs)
+    M, N = x.shape
+    kw = dict(dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = DualOutputs(torch.empty((M, N), **kw), torch.empty((M * N // 32,), **kw),
+                          torch.empty((N, M), **kw), torch.empty((N * M // 32,), **kw))
+    for name, t, n in zip(DualOutputs._fields, out, (M * N, M * N // 32, M * N, M * N // 32)):
+        _u8(t, n, name, x.device)
+    if workspace is None:
+        workspace = torch.empty((max(M * N // 32, 16),), **kw)
+    _check_cuda(workspace, "workspace")
+    with torch.cuda.device(x.device):
+        rc = lib().mxq_quantize_2d_dual_3pass(
+            ctypes.c_void_p(x.data_ptr()), M, N,
+            ctypes.c_void_p(offs.data_ptr() if offs is not None else 0), G,
+            *(ctypes.c_void_p(t.data_ptr()) for t in out),
+            ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+            _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_quantize_2d_dual_3pass")
     return out
 
 

@@ -213,6 +213,14 @@ __device__ __forceinline__ float e8m0_multiplier(uint32_t s) {
   return __uint_as_float(s == 255u ? 0x7FFFFFFFu : s == 254u ? 0x00400000u : (254u - s) << 23);
 }
 
+// Per-half max(|a|, |b|) of two bf16x2 words where a NaN operand loses to the
+// other one (IEEE maxNum); the sign bit is masked off by the caller.
+__device__ __forceinline__ uint32_t bf16x2_absmax_skip_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Per-half max(|a|, |b|) of two bf16x2 words, NaN-propagating (the sign bit of
 // the result is the xor of the inputs' signs and is masked off by the caller).
 __device__ __forceinline__ uint32_t bf16x2_absmax_nan(uint32_t a, uint32_t b) {

@@ -50,12 +50,23 @@ using namespace mxq;
 constexpr int kTile = 128;
 constexpr int kStages = MXQ_DUAL_STAGES;              // input ring depth (tiles)
 constexpr int kOutBufs = MXQ_DUAL_OUTBUFS;            // staged output tiles
-constexpr int kRowWarps = 8;                          // rowwise consumers
-constexpr int kConsumerWarps = 2 * kRowWarps;         // + as many colwise consumers
+constexpr int kPassWarps = 8;                         // consumer warps per pass
 constexpr int kGroupRows = MXQ_DUAL_GROUP_ROWS;       // tile rows per rasterization group
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kStoreWarp = kConsumerWarps + 1;
-constexpr int kThreads = (kConsumerWarps + 2) * 32;  // 576
+
+// What one launch computes: both passes (the fused cast), or one of them
+// alone (the separate 1x32 and 32x1 casts of the three-pass composition).
+enum Mode : int { kDual = 0, kRowOnly = 1, kColOnly = 2 };
+
+template <int kMode>
+struct Roles {
+  static constexpr bool kRow = kMode != kColOnly;
+  static constexpr bool kCol = kMode != kRowOnly;
+  static constexpr int kRowWarps = kRow ? kPassWarps : 0;  // warps [0, kRowWarps)
+  static constexpr int kConsumerWarps = kRowWarps + (kCol ? kPassWarps : 0);
+  static constexpr int kProducerWarp = kConsumerWarps;
+  static constexpr int kStoreWarp = kConsumerWarps + 1;
+  static constexpr int kThreads = (kConsumerWarps + 2) * 32;  // 576 for the fused cast
+};
 
 constexpr uint32_t kInStageBytes = kTile * kTile * 2;  // bf16 tile, 32 KiB
 constexpr uint32_t kHalfBytes = kTile * 64 * 2;        // [128 rows][64 bf16] box, 16 KiB
@@ -103,6 +114,16 @@ __device__ __forceinline__ uint32_t absmax_bits(const uint32_t* w) {
   uint32_t m = w[0];
 #pragma unroll
   for (int i = 1; i < kWords; ++i) m = bf16x2_absmax_nan(m, w[i]);
+  return m & 0x7FFF7FFFu;
+}
+
+// The same amax with NaN skipped (the separate 32x1 cast's rule): the running
+// maximum starts at 0 and a NaN operand never wins, so an all-NaN column gives 0.
+template <int kWords>
+__device__ __forceinline__ uint32_t absmax_bits_skip_nan(const uint32_t* w) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) m = bf16x2_absmax_skip_nan(m, w[i]);
   return m & 0x7FFF7FFFu;
 }
 
@@ -167,6 +188,7 @@ __device__ __forceinline__ void rowwise_pass(uint32_t in_s, uint32_t qrow_s, uin
 // of four consecutive rows of one column form one word: each lane emits 32
 // contiguous bytes of q_col per column.
 // ---------------------------------------------------------------------------
+template <bool kNaNPoisons>
 __device__ __forceinline__ void colwise_pass(uint32_t in_s, uint32_t qcol_s, uint32_t scol_s,
                                              int cwarp, int lane) {
   const int i = cwarp >> 1;
@@ -180,7 +202,7 @@ __device__ __forceinline__ void colwise_pass(uint32_t in_s, uint32_t qcol_s, uin
 #pragma unroll
   for (int j = 0; j < 32; ++j) w[j] = lds32(half + swz(32 * i + j, chunk) + within);
 
-  const uint32_t m = absmax_bits<32>(w);
+  const uint32_t m = kNaNPoisons ? absmax_bits<32>(w) : absmax_bits_skip_nan<32>(w);
   const uint32_t s_lo = e8m0_rceil_from_bits(m & 0xFFFFu, 254u);  // column 2p
   const uint32_t s_hi = e8m0_rceil_from_bits(m >> 16, 254u);      // column 2p+1
   const float mult_lo = e8m0_multiplier(s_lo);
@@ -237,12 +259,18 @@ __device__ __forceinline__ int group_of_row(const int32_t* s_offs, int G, int64_
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    mxq_dual_kernel(const __grid_constant__ CUtensorMap tm_x,
+// One persistent launch over all 128x128 tiles.  kDual: the fused cast
+// (q_row, s_row, q_col and grouped s_col).  kRowOnly: q_row and s_row.
+// kColOnly: q_col and the colwise scales as a plain [N, M/32] row-major matrix
+// written to `s_col` (the separate 32x1 cast, NaN skipped by its amax).
+template <int kMode>
+__global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
+    mxq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_qrow,
                     const __grid_constant__ CUtensorMap tm_qcol, const int32_t* __restrict__ offs,
                     int G, int M, int N, uint8_t* __restrict__ s_row,
                     uint8_t* __restrict__ s_col) {
+  using R = Roles<kMode>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -264,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bars.full(s), 1);
-      mbar_init(bars.empty(s), kConsumerWarps);
+      mbar_init(bars.empty(s), R::kConsumerWarps);
     }
     for (int b = 0; b < kOutBufs; ++b) {
-      mbar_init(bars.ofull(b), kConsumerWarps);
+      mbar_init(bars.ofull(b), R::kConsumerWarps);
       mbar_init(bars.oempty(b), 1);
     }
     *abort_flag = 0u;
@@ -281,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Producer prologue: start the first loads before the offsets check.
   int64_t issued = 0;
-  const bool is_producer = (warp == kProducerWarp) && (lane == 0);
+  const bool is_producer = (warp == R::kProducerWarp) && (lane == 0);
   auto issue_load = [&](int64_t k) {
     int64_t ti, tj;
     tile_coords(blockIdx.x + k * static_cast<int64_t>(gridDim.x), TM, TN, &ti, &tj);
@@ -302,13 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; issued < my_tiles && issued < kStages; ++issued) issue_load(issued);
   }
 
-  // Device-side check of the group offsets: ascending, multiples of 128,
-  // within [0, M].  Every CTA reaches the same verdict; on failure nothing is
-  // written and the status word records it.
+  // Device-side check of the group offsets (fused cast only): ascending,
+  // multiples of 128, within [0, M].  Every CTA reaches the same verdict; on
+  // failure nothing is written and the status word records it.
   int64_t end_rows = M;
-  if (offs != nullptr) {
+  if (kMode == kDual && offs != nullptr) {
     int bad = 0;
-    for (int g = tid; g < G; g += kThreads) {
+    for (int g = tid; g < G; g += R::kThreads) {
       const int32_t v = offs[g];
       const int32_t prev = g ? offs[g - 1] : 0;
       if (v < prev || (v & (kTile - 1)) != 0 || v > M) bad = 1;
@@ -323,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     end_rows = s_offs[G - 1];
   }
 
-  if (warp < kConsumerWarps) {
+  if (warp < R::kConsumerWarps) {
     // ------------------------------------------------------------- consumers
     for (int64_t k = 0; k < my_tiles; ++k) {
       const int s = static_cast<int>(k % kStages);
@@ -337,19 +365,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT);
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       const uint32_t in_s = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
-      if (warp < kRowWarps)
+      if (warp < R::kRowWarps)
         rowwise_pass(in_s, base + kOffQRow + b * kQTileBytes, base + kOffSRow + b * kAtomBytes,
                      warp, lane);
       else
-        colwise_pass(in_s, base + kOffQCol + b * kQTileBytes, base + kOffSCol + b * kAtomBytes,
-                     warp - kRowWarps, lane);
+        colwise_pass<kMode == kDual>(in_s, base + kOffQCol + b * kQTileBytes,
+                                     base + kOffSCol + b * kAtomBytes, warp - R::kRowWarps, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.empty(s));
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.ofull(b));
     }
-  } else if (warp == kProducerWarp) {
+  } else if (warp == R::kProducerWarp) {
     // -------------------------------------------------------------- producer
     if (lane == 0) {
       for (int64_t k = issued; k < my_tiles; ++k) {
@@ -363,48 +391,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = k + 1;
       }
     }
-  } else if (warp == kStoreWarp) {
+  } else if (warp == R::kStoreWarp) {
     // ---------------------------------------------------------------- storer
+    // Lane 0 issues the TMA and bulk stores.  For the 32x1 cast every lane
+    // also copies the tile's 128 scale words (4 row blocks of one column are
+    // adjacent in the staged atom) into the row-major scale matrix.
+    if (kMode != kColOnly && lane != 0) return;
     if (lane == 0) {
-      tma_prefetch_desc(&tm_qrow);
-      tma_prefetch_desc(&tm_qcol);
-      const int64_t Mrows = M;
-      for (int64_t k = 0; k < my_tiles; ++k) {
-        const int b = static_cast<int>(k % kOutBufs);
-        if (!mbar_wait_bounded(bars.ofull(b), static_cast<uint32_t>((k / kOutBufs) & 1), abort_flag,
-                               &g_mxq_status, MXQ_DEV_TIMEOUT))
-          break;
-        int64_t ti, tj;
-        tile_coords(blockIdx.x + k * static_cast<int64_t>(gridDim.x), TM, TN, &ti, &tj);
-        const int64_t row0 = ti * kTile;
-        tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
-                     base + kOffQRow + b * kQTileBytes);
-        tma_store_2d(&tm_qcol, static_cast<int32_t>(row0), static_cast<int32_t>(tj * kTile),
-                     base + kOffQCol + b * kQTileBytes);
-        bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
-                   kAtomBytes);
-        if (row0 < end_rows) {
-          int64_t lo = 0, hi = Mrows;
-          if (offs != nullptr) {
-            const int g = group_of_row(s_offs, G, row0);
-            lo = g ? s_offs[g - 1] : 0;
-            hi = s_offs[g];
+      if (R::kRow) tma_prefetch_desc(&tm_qrow);
+      if (R::kCol) tma_prefetch_desc(&tm_qcol);
+    }
+    const int64_t Mrows = M;
+    for (int64_t k = 0; k < my_tiles; ++k) {
+      const int b = static_cast<int>(k % kOutBufs);
+      bool ok = mbar_wait_bounded(bars.ofull(b), static_cast<uint32_t>((k / kOutBufs) & 1),
+                                  abort_flag, &g_mxq_status, MXQ_DEV_TIMEOUT);
+      if (kMode == kColOnly) ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      int64_t ti, tj;
+      tile_coords(blockIdx.x + k * static_cast<int64_t>(gridDim.x), TM, TN, &ti, &tj);
+      const int64_t row0 = ti * kTile;
+      if (kMode == kColOnly) {
+        const int64_t pitch = Mrows / 32;  // bytes per row of the [N, M/32] matrix
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int n = lane + 32 * r;
+          const uint32_t word =
+              lds32(base + kOffSCol + b * kAtomBytes + static_cast<uint32_t>((n & 31) * 16 + (n >> 5) * 4));
+          *reinterpret_cast<uint32_t*>(s_col + (tj * kTile + n) * pitch + 4 * ti) = word;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        if (R::kRow) {
+          tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
+                       base + kOffQRow + b * kQTileBytes);
+          bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
+                     kAtomBytes);
+        }
+        if (R::kCol)
+          tma_store_2d(&tm_qcol, static_cast<int32_t>(row0), static_cast<int32_t>(tj * kTile),
+                       base + kOffQCol + b * kQTileBytes);
+        if (kMode == kDual) {
+          if (row0 < end_rows) {
+            int64_t lo = 0, hi = Mrows;
+            if (offs != nullptr) {
+              const int g = group_of_row(s_offs, G, row0);
+              lo = g ? s_offs[g - 1] : 0;
+              hi = s_offs[g];
+            }
+            const int64_t atoms_per_nblock = (hi - lo) / kTile;  // (hi-lo)/32 scale cols / 4
+            uint8_t* dst = s_col + static_cast<int64_t>(N) * lo / 32 +
+                           (tj * atoms_per_nblock + (row0 - lo) / kTile) * kAtomBytes;
+            bulk_store(dst, base + kOffSCol + b * kAtomBytes, kAtomBytes);
+          } else {
+            uint8_t* dst = s_col + static_cast<int64_t>(N) * end_rows / 32 +
+                           (((row0 - end_rows) / kTile) * TN + tj) * kAtomBytes;
+            bulk_store(dst, base + kOffZero, kAtomBytes);
           }
-          const int64_t atoms_per_nblock = (hi - lo) / kTile;  // (hi-lo)/32 scale cols / 4
-          uint8_t* dst = s_col + static_cast<int64_t>(N) * lo / 32 +
-                         (tj * atoms_per_nblock + (row0 - lo) / kTile) * kAtomBytes;
-          bulk_store(dst, base + kOffSCol + b * kAtomBytes, kAtomBytes);
-        } else {
-          uint8_t* dst = s_col + static_cast<int64_t>(N) * end_rows / 32 +
-                         (((row0 - end_rows) / kTile) * TN + tj) * kAtomBytes;
-          bulk_store(dst, base + kOffZero, kAtomBytes);
         }
         bulk_commit();
         bulk_wait_read<0>();
         mbar_arrive(bars.oempty(b));
       }
-      bulk_wait_all<0>();
     }
+    if (lane == 0) bulk_wait_all<0>();
   }
 }
 
@@ -438,13 +489,14 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool ensure_dual_smem_attr(int dev) {
+template <int kMode>
+bool ensure_smem_attr(int dev) {
   static std::mutex mu;
   static bool done[64] = {};
   if (dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(mxq_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mxq_tile_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return false;
     done[dev] = true;
@@ -452,13 +504,55 @@ bool ensure_dual_smem_attr(int dev) {
   return true;
 }
 
+int check_shape(int64_t M, int64_t N) {
+  if (M < 0 || N < 0 || M % kTile != 0 || N % kTile != 0 || M > INT32_MAX || N > INT32_MAX)
+    return MXQ_EBADSHAPE;
+  return MXQ_OK;
+}
+
+// Encode the tensor maps (unused ones get a valid map of x) and launch one
+// persistent wave: min(tiles, SMs) CTAs.
+template <int kMode>
+int launch_tiles(const void* x, int64_t M, int64_t N, const int32_t* offs, int32_t G,
+                 uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                 cudaStream_t stream) {
+  int dev = 0;
+  const int sms = sm_count_current_device(&dev);
+  if (sms <= 0 || !ensure_smem_attr<kMode>(dev)) return MXQ_ECUDA;
+  CUtensorMap tm_x, tm_qrow, tm_qcol;
+  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, N, M, 2ull * N, 64, kTile))
+    return MXQ_ECUDA;
+  if (q_row) {
+    if (!encode_2d(&tm_qrow, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, N, M, N, kTile, kTile))
+      return MXQ_ECUDA;
+  } else {
+    tm_qrow = tm_x;
+  }
+  if (q_col) {
+    if (!encode_2d(&tm_qcol, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, M, N, M, kTile, kTile))
+      return MXQ_ECUDA;
+  } else {
+    tm_qcol = tm_x;
+  }
+  const int64_t T = (M / kTile) * (N / kTile);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T < sms ? T : sms));
+  cfg.blockDim = dim3(Roles<kMode>::kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, mxq_tile_kernel<kMode>, tm_x, tm_qrow, tm_qcol, offs,
+                         static_cast<int>(G), static_cast<int>(M), static_cast<int>(N), s_row, s_col);
+  return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
+}
+
 }  // namespace
 
 extern "C" int mxq_quantize_2d_dual(const void* x, int64_t M, int64_t N, const int32_t* offs,
                                     int32_t G, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                                     uint8_t* s_col, cudaStream_t stream) {
-  if (M < 0 || N < 0 || M % kTile != 0 || N % kTile != 0 || M > INT32_MAX || N > INT32_MAX)
-    return MXQ_EBADSHAPE;
+  int rc = check_shape(M, N);
+  if (rc != MXQ_OK) return rc;
   if (offs == nullptr ? G != 0 : (G < 1 || G > MXQ_MAX_GROUPS)) return MXQ_EBADOFFS;
   if (offs != nullptr && !aligned_to(offs, 4)) return MXQ_EALIGN;
   if (M == 0 || N == 0) return MXQ_OK;
@@ -476,31 +570,42 @@ extern "C" int mxq_quantize_2d_dual(const void* x, int64_t M, int64_t N, const i
       {reinterpret_cast<uintptr_t>(offs), offs ? 4ull * static_cast<uint64_t>(G) : 0ull},
   };
   if (ranges_overlap(r, 6)) return MXQ_EOVERLAP;
+  return launch_tiles<kDual>(x, M, N, offs, G, q_row, s_row, q_col, s_col, stream);
+}
 
-  int dev = 0;
-  const int sms = sm_count_current_device(&dev);
-  if (sms <= 0 || !ensure_dual_smem_attr(dev)) return MXQ_ECUDA;
+extern "C" int mxq_quantize_1x32(const void* x, int64_t M, int64_t N, uint8_t* q_row,
+                                 uint8_t* s_row, cudaStream_t stream) {
+  int rc = check_shape(M, N);
+  if (rc != MXQ_OK) return rc;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!x || !q_row || !s_row) return MXQ_ENULL;
+  if (!aligned_to(x, 16) || !aligned_to(q_row, 16) || !aligned_to(s_row, 16)) return MXQ_EALIGN;
+  const uint64_t MN = static_cast<uint64_t>(M) * static_cast<uint64_t>(N);
+  const ByteRange r[3] = {{reinterpret_cast<uintptr_t>(x), 2 * MN},
+                          {reinterpret_cast<uintptr_t>(q_row), MN},
+                          {reinterpret_cast<uintptr_t>(s_row), MN / 32}};
+  if (ranges_overlap(r, 3)) return MXQ_EOVERLAP;
+  return launch_tiles<kRowOnly>(x, M, N, nullptr, 0, q_row, s_row, nullptr, nullptr, stream);
+}
 
-  CUtensorMap tm_x, tm_qrow, tm_qcol;
-  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, N, M, 2ull * N, 64, kTile) ||
-      !encode_2d(&tm_qrow, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, N, M, N, kTile, kTile) ||
-      !encode_2d(&tm_qcol, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, M, N, M, kTile, kTile))
-    return MXQ_ECUDA;
-
-  const int64_t T = (M / kTile) * (N / kTile);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(T < sms ? T : sms));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, mxq_dual_kernel, tm_x, tm_qrow, tm_qcol, offs, static_cast<int>(G),
-                         static_cast<int>(M), static_cast<int>(N), s_row, s_col);
-  return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
+extern "C" int mxq_quantize_32x1(const void* x, int64_t M, int64_t N, uint8_t* q_col,
+                                 uint8_t* s_rm, cudaStream_t stream) {
+  int rc = check_shape(M, N);
+  if (rc != MXQ_OK) return rc;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!x || !q_col || !s_rm) return MXQ_ENULL;
+  if (!aligned_to(x, 16) || !aligned_to(q_col, 16) || !aligned_to(s_rm, 16)) return MXQ_EALIGN;
+  const uint64_t MN = static_cast<uint64_t>(M) * static_cast<uint64_t>(N);
+  const ByteRange r[3] = {{reinterpret_cast<uintptr_t>(x), 2 * MN},
+                          {reinterpret_cast<uintptr_t>(q_col), MN},
+                          {reinterpret_cast<uintptr_t>(s_rm), MN / 32}};
+  if (ranges_overlap(r, 3)) return MXQ_EOVERLAP;
+  return launch_tiles<kColOnly>(x, M, N, nullptr, 0, nullptr, nullptr, q_col, s_rm, stream);
 }
 
 namespace mxq {
-int mx9_status_read(unsigned int* out, bool clear);  // mx9.cu
+int mx9_status_read(unsigned int* out, bool clear);      // mx9.cu
+int compose_status_read(unsigned int* out, bool clear);  // mxq_compose.cu
 }
 
 // The device status word is the OR of the per-file words of the kernels.
@@ -512,8 +617,11 @@ extern "C" int mxq_device_status(uint32_t* out, int clear) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_mxq_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ECUDA;
   }
-  const int rc = mxq::mx9_status_read(&w, clear != 0);
+  unsigned int c = 0;
+  int rc = mxq::mx9_status_read(&w, clear != 0);
   if (rc != MXQ_OK) return rc;
-  *out = v | w;
+  rc = mxq::compose_status_read(&c, clear != 0);
+  if (rc != MXQ_OK) return rc;
+  *out = v | w | c;
   return MXQ_OK;
 }

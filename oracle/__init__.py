@@ -79,6 +79,14 @@ def _lib():
         lib.oracle_mx9_pack.argtypes = [p, ctypes.c_int, i64, i64, p, p, p]
         lib.oracle_mx9_unpack.restype = ctypes.c_int
         lib.oracle_mx9_unpack.argtypes = [p, p, p, p, ctypes.c_int, i64, i64]
+        lib.oracle_mxfp8_block_nan_dropped.restype = None
+        lib.oracle_mxfp8_block_nan_dropped.argtypes = [p, i64, p, p, i64]
+        lib.oracle_mxfp8_1x32.restype = ctypes.c_int
+        lib.oracle_mxfp8_1x32.argtypes = [p, i64, i64, p, p]
+        lib.oracle_mxfp8_32x1.restype = ctypes.c_int
+        lib.oracle_mxfp8_32x1.argtypes = [p, i64, i64, p, p]
+        lib.oracle_swizzle_kgroups.restype = ctypes.c_int
+        lib.oracle_swizzle_kgroups.argtypes = [p, i64, i64, p, ctypes.c_int32, p]
         lib.oracle_rounding_is_nearest_even.restype = ctypes.c_int
         lib.oracle_rounding_is_nearest_even.argtypes = []
         if not lib.oracle_rounding_is_nearest_even():
@@ -133,6 +141,16 @@ def mxfp8_block(values_bf16_bits: np.ndarray, colwise: bool) -> tuple[int, np.nd
     s = np.zeros(1, np.uint8)
     q = np.zeros(32, np.uint8)
     _lib().oracle_mxfp8_block(_ptr(x), 1, int(bool(colwise)), _ptr(s), _ptr(q), 1)
+    return int(s[0]), q
+
+
+def mxfp8_block_nan_dropped(values_bf16_bits: np.ndarray) -> tuple[int, np.ndarray]:
+    """The separate 32x1 cast's block rule (NaN skipped by the amax, Inf saturates)."""
+    x = np.ascontiguousarray(values_bf16_bits, dtype=np.uint16)
+    assert x.size == 32
+    s = np.zeros(1, np.uint8)
+    q = np.zeros(32, np.uint8)
+    _lib().oracle_mxfp8_block_nan_dropped(_ptr(x), 1, _ptr(s), _ptr(q), 1)
     return int(s[0]), q
 
 
@@ -206,3 +224,50 @@ def mx9_unpack(q: np.ndarray, max_exp: np.ndarray, prime: np.ndarray, out_dtype:
     if rc != OK:
         raise OracleError(rc)
     return y
+
+
+# --------------------------------------------------------------------------
+# the three-pass composition (1x32 cast, 32x1 cast, K-groups swizzle)
+# --------------------------------------------------------------------------
+
+def mxfp8_1x32(x_bits: np.ndarray) -> dict[str, np.ndarray]:
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, N = x.shape
+    q_row = np.empty(M * N, np.uint8)
+    s_row = np.empty(M * N // 32, np.uint8)
+    rc = _lib().oracle_mxfp8_1x32(_ptr(x), M, N, _ptr(q_row), _ptr(s_row))
+    if rc != OK:
+        raise OracleError(rc)
+    return {"q_row": q_row, "s_row": s_row}
+
+
+def mxfp8_32x1(x_bits: np.ndarray) -> dict[str, np.ndarray]:
+    """q_col [N*M] and the plain row-major colwise scales s_rm [N, M/32]."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, N = x.shape
+    q_col = np.empty(M * N, np.uint8)
+    s_rm = np.empty((N, M // 32), np.uint8)
+    rc = _lib().oracle_mxfp8_32x1(_ptr(x), M, N, _ptr(q_col), _ptr(s_rm))
+    if rc != OK:
+        raise OracleError(rc)
+    return {"q_col": q_col, "s_rm": s_rm}
+
+
+def swizzle_kgroups(s_rm: np.ndarray, offs: np.ndarray | None) -> np.ndarray:
+    s = np.ascontiguousarray(s_rm, dtype=np.uint8)
+    N, C = s.shape
+    M = 32 * C
+    o = None if offs is None else np.ascontiguousarray(offs, dtype=np.int32)
+    out = np.empty(N * M // 32, np.uint8)
+    rc = _lib().oracle_swizzle_kgroups(_ptr(s), N, M, _ptr(o), 0 if o is None else o.size, _ptr(out))
+    if rc != OK:
+        raise OracleError(rc)
+    return out
+
+
+def mxfp8_dual_3pass(x_bits: np.ndarray, offs: np.ndarray | None = None) -> dict[str, np.ndarray]:
+    """What the three separate passes produce together."""
+    r = mxfp8_1x32(x_bits)
+    c = mxfp8_32x1(x_bits)
+    return {"q_row": r["q_row"], "s_row": r["s_row"], "q_col": c["q_col"],
+            "s_col": swizzle_kgroups(c["s_rm"], offs), "s_rm": c["s_rm"].reshape(-1)}

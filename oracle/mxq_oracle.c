@@ -175,6 +175,34 @@ void oracle_mxfp8_block(const uint16_t *x, int64_t stride, int colwise,
     }
 }
 
+/*
+ * The colwise block of the separate 32x1 cast that the fused kernel replaces
+ * ([AO] description, NaN paragraph): its amax skips NaN entirely, so a block
+ * holding NaN still gets the scale its other elements imply (0 when every
+ * element is NaN: the maximum over no values is taken as 0, READING); the
+ * cast saturates, so +-Inf gives scale 254 and +-448 data, and a NaN element
+ * stays a NaN byte (0x7F).
+ */
+void oracle_mxfp8_block_nan_dropped(const uint16_t *x, int64_t stride, uint8_t *scale_out,
+                                    uint8_t *q, int64_t qstride) {
+    int any_inf = 0, s, i;
+    double amax = 0.0;
+    for (i = 0; i < 32; ++i) {
+        double v = bf16_to_double(x[i * stride]);
+        if (isnan(v)) continue;
+        if (isinf(v))
+            any_inf = 1;
+        else if (fabs(v) > amax)
+            amax = fabs(v);
+    }
+    s = any_inf ? 254 : oracle_e8m0_rceil(amax);
+    *scale_out = (uint8_t)s;
+    for (i = 0; i < 32; ++i) {
+        double v = bf16_to_double(x[i * stride]);
+        q[i * qstride] = isnan(v) ? 0x7F : oracle_e4m3_encode(ldexp(v, 127 - s));
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Blocked scale layout                                                       */
 /* ------------------------------------------------------------------------- */
@@ -278,6 +306,61 @@ int oracle_mxfp8_dual(const uint16_t *x, int64_t M, int64_t N,
             }
         }
         for (b = N * end / 32; b < N * M / 32; ++b) s_col[b] = 0;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The three-pass composition ([AO] description, first paragraph): a 1x32     */
+/* cast, a 32x1 cast with plain row-major scales, and a K-groups swizzle of   */
+/* those scales into the blocked per-group slabs.                             */
+/* ------------------------------------------------------------------------- */
+
+/* 1x32 pass: q_row and s_row exactly as in oracle_mxfp8_dual. */
+int oracle_mxfp8_1x32(const uint16_t *x, int64_t M, int64_t N, uint8_t *q_row, uint8_t *s_row) {
+    int64_t m, j;
+    if (M < 0 || N < 0 || M % 128 != 0 || N % 128 != 0) return ORC_EBADSHAPE;
+    for (m = 0; m < M; ++m)
+        for (j = 0; j < N / 32; ++j) {
+            uint8_t s;
+            oracle_mxfp8_block(x + m * N + 32 * j, 1, 0, &s, q_row + m * N + 32 * j, 1);
+            s_row[oracle_blocked_index(m, j, M, N / 32)] = s;
+        }
+    return ORC_OK;
+}
+
+/* 32x1 pass: q_col[n*M + m] and the scales as a plain [N, M/32] row-major
+   matrix s_rm[n*(M/32) + i], with the NaN-dropping block rule above. */
+int oracle_mxfp8_32x1(const uint16_t *x, int64_t M, int64_t N, uint8_t *q_col, uint8_t *s_rm) {
+    int64_t i, n;
+    if (M < 0 || N < 0 || M % 128 != 0 || N % 128 != 0) return ORC_EBADSHAPE;
+    for (i = 0; i < M / 32; ++i)
+        for (n = 0; n < N; ++n)
+            oracle_mxfp8_block_nan_dropped(x + 32 * i * N + n, N, &s_rm[n * (M / 32) + i],
+                                           q_col + n * M + 32 * i, 1);
+    return ORC_OK;
+}
+
+/* K-groups swizzle: s_rm [N, M/32] row-major -> s_col with group g's columns
+   [lo/32, hi/32) blocked as one slab at byte N*lo/32, and zeros from
+   N*offs[G-1]/32 on (the separate pass "iterates groups and returns
+   new_zeros", [AO] "Uncovered tail" paragraph).  offs == NULL: one group. */
+int oracle_swizzle_kgroups(const uint8_t *s_rm, int64_t N, int64_t M, const int32_t *offs,
+                           int32_t G, uint8_t *s_col) {
+    int64_t b, n, c, lo = 0;
+    int32_t g, ng = offs ? G : 1;
+    int rc;
+    if (M < 0 || N < 0 || M % 128 != 0 || N % 128 != 0) return ORC_EBADSHAPE;
+    rc = oracle_check_offs(offs, G, M);
+    if (rc != ORC_OK) return rc;
+    for (b = 0; b < N * M / 32; ++b) s_col[b] = 0;
+    for (g = 0; g < ng; ++g) {
+        int64_t hi = offs ? offs[g] : M;
+        for (n = 0; n < N; ++n)
+            for (c = lo / 32; c < hi / 32; ++c)
+                s_col[N * lo / 32 + oracle_blocked_index(n, c - lo / 32, N, (hi - lo) / 32)] =
+                    s_rm[n * (M / 32) + c];
+        lo = hi;
     }
     return ORC_OK;
 }

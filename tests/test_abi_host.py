@@ -126,3 +126,32 @@ def test_valid_call_without_gpu_fails_loudly(L):
     """With no GPU the first CUDA call fails and the library reports it (no CPU fallback)."""
     assert _dual(L) == mxq.ECUDA
     assert _pack(L) == mxq.ECUDA
+
+
+def test_composition_rejections(L):
+    vp = ctypes.c_void_p
+    M = N = 128
+    MN = M * N
+    ok = dict(x=A, qr=A + 4 * MN, sr=A + 6 * MN, qc=A + 8 * MN, sc=A + 10 * MN, ws=A + 12 * MN)
+
+    def three(x=None, ws=None, wsb=MN // 32, M=M, N=N, offs=None, G=0):
+        a = dict(ok)
+        if x is not None:
+            a["x"] = x
+        if ws is not None:
+            a["ws"] = ws
+        return L.mxq_quantize_2d_dual_3pass(vp(a["x"]), M, N, vp(offs), G, vp(a["qr"]), vp(a["sr"]),
+                                            vp(a["qc"]), vp(a["sc"]), vp(a["ws"]), wsb, None)
+    assert three(M=100) == mxq.EBADSHAPE
+    assert three(wsb=MN // 32 - 1) == mxq.EBADSHAPE
+    assert three(ws=0) == mxq.ENULL
+    assert three(ws=A + 12 * MN + 8) == mxq.EALIGN
+    assert three(ws=A + 4 * MN + 16) == mxq.EOVERLAP     # workspace inside q_row
+    assert three(offs=None, G=2) == mxq.EBADOFFS
+    assert L.mxq_quantize_1x32(vp(A), 96, 128, vp(A + 4 * MN), vp(A + 6 * MN), None) == mxq.EBADSHAPE
+    assert L.mxq_quantize_1x32(vp(A), M, N, vp(A + 16), vp(A + 6 * MN), None) == mxq.EOVERLAP
+    assert L.mxq_quantize_32x1(vp(A), M, N, vp(0), vp(A + 6 * MN), None) == mxq.ENULL
+    assert L.mxq_quantize_32x1(vp(A), M, N, vp(A + 4 * MN), vp(A + 4 * MN + 16), None) == mxq.EOVERLAP
+    assert L.mxq_swizzle_kgroups(vp(A), N, M, vp(0), 1, vp(A + MN), None) == mxq.EBADOFFS
+    assert L.mxq_swizzle_kgroups(vp(A), N, M, vp(0), 0, vp(A + 16), None) == mxq.EOVERLAP
+    assert L.mxq_swizzle_kgroups(vp(A), 0, M, vp(0), 0, vp(0), None) == mxq.OK

@@ -181,7 +181,10 @@ def test_block_golden(line):
     want = np.full(32, int(dfill, 16), np.uint8)
     for k, v in _parse_overrides(dover).items():
         want[k] = v
-    s, q = oracle.mxfp8_block(x, colwise=(axis == "col"))
+    if axis == "col32x1":
+        s, q = oracle.mxfp8_block_nan_dropped(x)
+    else:
+        s, q = oracle.mxfp8_block(x, colwise=(axis == "col"))
     assert s == int(scale)
     np.testing.assert_array_equal(q, want)
 
@@ -378,3 +381,67 @@ def test_bytes_per_element_closed_form():
     # three kernels: two reads of x, the four outputs, and a read+write of the
     # colwise scales by the separate swizzle pass
     assert (2 * 2 * M * N + sum(v.size for v in out.values()) + 2 * (M * N // 32)) / (M * N) == 6.125
+
+
+# ---------------------------------------------------------------------------
+# the three-pass composition the fused cast replaces
+# ---------------------------------------------------------------------------
+
+def test_nan_dropped_rule_equals_colwise_rule_without_nan():
+    """With no NaN in the block the separate 32x1 cast and the fused colwise
+    rule agree (the page: the only divergence is NaN on the colwise output)."""
+    g = np.random.Generator(np.random.PCG64(12))
+    for _ in range(300):
+        x = W.f32_to_bf16_bits((g.standard_normal(32) * 2.0 ** int(g.integers(-130, 120)))
+                               .astype(np.float32))
+        if g.random() < 0.3:
+            x[int(g.integers(32))] = 0x7F80 | (int(g.integers(2)) << 15)
+        a = oracle.mxfp8_block(x, True)
+        b = oracle.mxfp8_block_nan_dropped(x)
+        assert a[0] == b[0]
+        np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("M,N,offs", [(256, 384, None), (512, 256, [0, 128, 128, 384]),
+                                      (384, 128, [384]), (256, 256, [0])])
+def test_swizzle_matches_reshape_blocking(M, N, offs):
+    """The swizzle's slabs equal the reshape statement of the blocked layout
+    applied to each group's columns; the tail is zero."""
+    g = np.random.Generator(np.random.PCG64(M + N))
+    s_rm = g.integers(0, 256, size=(N, M // 32), dtype=np.uint8)
+    o = None if offs is None else np.array(offs, np.int32)
+    out = oracle.swizzle_kgroups(s_rm, o)
+    ends = [M] if offs is None else offs
+    lo = 0
+    for hi in ends:
+        if hi > lo:
+            want = _blocked_by_reshape(torch.from_numpy(np.ascontiguousarray(s_rm[:, lo // 32:hi // 32]))).numpy()
+            np.testing.assert_array_equal(out[N * lo // 32:N * hi // 32], want)
+        lo = hi
+    assert not out[N * ends[-1] // 32:].any()
+
+
+def test_three_pass_equals_fused_except_nan_columns():
+    """The composition matches the fused cast byte for byte except in colwise
+    blocks holding NaN, where the fused cast poisons (255, all 0x7F) and the
+    composition keeps the other elements' scale."""
+    M, N = 256, 256
+    x = W.normal_bf16((M, N), seed=21)
+    x[5, 7] = 0x7FC0          # NaN: row block (5, 0), column block (0, 7)
+    x[100, 200] = 0x7F80      # +Inf: both rules agree
+    offs = np.array([128, 256], np.int32)
+    a = oracle.mxfp8_dual(x, offs)
+    b = oracle.mxfp8_dual_3pass(x, offs)
+    for k in ("q_row", "s_row"):
+        np.testing.assert_array_equal(a[k], b[k])
+    qa, qb = a["q_col"].reshape(N, M), b["q_col"].reshape(N, M)
+    diff = np.argwhere(qa != qb)
+    assert diff.size and set(map(tuple, diff[:, :1].tolist())) == {(7,)}
+    assert np.all((diff[:, 1] >= 0) & (diff[:, 1] < 32))
+    assert (qa[7, :32] == 0x7F).all() and qb[7, 5] == 0x7F and (qb[7, :32] != 0x7F).sum() == 31
+    sa = _unblock_by_reshape(a["s_col"][:N * 128 // 32], N, 4)
+    sb = _unblock_by_reshape(b["s_col"][:N * 128 // 32], N, 4)
+    assert sa[7, 0] == 255 and sb[7, 0] < 255
+    sa[7, 0] = sb[7, 0]
+    np.testing.assert_array_equal(sa, sb)
+    np.testing.assert_array_equal(a["s_col"][N * 128 // 32:], b["s_col"][N * 128 // 32:])
