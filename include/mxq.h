@@ -46,6 +46,7 @@ typedef struct CUstream_st *cudaStream_t;
 #define MXQ_EOVERLAP (-5)  /* two buffers' byte ranges overlap */
 #define MXQ_ECUDA (-6)     /* the CUDA runtime refused the launch */
 #define MXQ_ENULL (-7)     /* a required pointer is NULL */
+#define MXQ_ESCRATCH (-8)  /* needs more than the static scratch of the no-allocation call */
 
 /* ---- dtype codes ------------------------------------------------------- */
 #define MXQ_F32 0
@@ -166,6 +167,31 @@ int mxq_swizzle_kgroups(const uint8_t *s_rm, int64_t N, int64_t M, const int32_t
 int mxq_quantize_2d_dual_3pass(const void *x, int64_t M, int64_t N, const int32_t *offs, int32_t G,
                                uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
                                uint8_t *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * mxq_quantize_2d_dual_3pass without any allocation.  The pages have no
+ * counterpart: this is a library convenience.  It is for callers that cannot
+ * allocate device memory when they need the cast -- work recorded into a CUDA
+ * graph in global capture mode (allocation is illegal there), latency-critical
+ * paths where cudaMalloc/cudaFree can synchronize the device, and plugins inside
+ * a framework that owns all device memory through an allocator they cannot
+ * reach.  The three passes' workspace is a static device array of
+ * MXQ_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library holds until the process exits; the call makes no cudaMalloc or
+ * cudaFree and calls no allocating routine.
+ *   Arguments, outputs and errors as mxq_quantize_2d_dual_3pass minus the
+ *   workspace; returns MXQ_ESCRATCH, enqueuing nothing, when M*N/32 exceeds
+ *   MXQ_NOALLOC_SCRATCH_BYTES (16 MiB: M*N up to 2^29 elements).
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   All calls share the one array and each overwrites the part it uses before
+ *   reading it: calls that may overlap on the GPU (different streams without
+ *   ordering between them) race on it and must be serialized by the caller.
+ */
+#define MXQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+int mxq_quantize_2d_dual_3pass_noalloc(const void *x, int64_t M, int64_t N, const int32_t *offs,
+                                       int32_t G, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
+                                       uint8_t *s_col, cudaStream_t stream);
 
 /*
  * Device status word of the current device: a sticky OR of MXQ_DEV_* bits set

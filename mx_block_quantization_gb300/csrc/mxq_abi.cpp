@@ -11,6 +11,9 @@ extern "C" const char* mxq_status_string(int status) {
     case MXQ_EOVERLAP: return "overlapping buffers";
     case MXQ_ECUDA: return "CUDA runtime error at launch";
     case MXQ_ENULL: return "NULL pointer for a non-empty buffer";
+    case MXQ_ESCRATCH:
+      return "problem needs more scratch than the static area of the no-allocation call "
+             "(M*N/32 > MXQ_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

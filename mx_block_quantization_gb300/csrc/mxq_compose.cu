@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "mxq.h"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
@@ -188,4 +190,59 @@ extern "C" int mxq_quantize_2d_dual_3pass(const void* x, int64_t M, int64_t N,
   rc = mxq_quantize_32x1(x, M, N, q_col, workspace, stream);
   if (rc != MXQ_OK) return rc;
   return launch_swizzle(workspace, N, M, offs, G, s_col, stream);
+}
+
+// ---------------------------------------------------------------------------
+// The same three passes without any allocation by anyone.
+//
+// Some callers cannot allocate device memory at the moment they need this cast:
+// work being recorded into a CUDA graph in global capture mode (allocation
+// calls are illegal during such a capture), latency-critical paths where a
+// cudaMalloc/cudaFree can synchronize the device, and plugins running inside a
+// framework that owns all device memory through its own allocator, which the
+// plugin cannot reach.  For them the workspace of the three-pass call lives in
+// a static device array of this library instead of a caller buffer.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Holds the row-major colwise scales between the 32x1 pass and the swizzle.
+// Every GPU that loads this library keeps it until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MXQ_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the array on device `dev`, looked up once per device with
+// that device current (the host-side name is only a stand-in for the symbol).
+uint8_t* noalloc_scratch(int dev) {
+  static std::mutex mu;
+  static uint8_t* addr[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint8_t*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int mxq_quantize_2d_dual_3pass_noalloc(const void* x, int64_t M, int64_t N,
+                                                  const int32_t* offs, int32_t G, uint8_t* q_row,
+                                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                                  cudaStream_t stream) {
+  if (M < 0 || N < 0 || M % 128 != 0 || N % 128 != 0 || M > INT32_MAX || N > INT32_MAX)
+    return MXQ_EBADSHAPE;
+  if (offs == nullptr ? G != 0 : (G < 1 || G > MXQ_MAX_GROUPS)) return MXQ_EBADOFFS;
+  if (offs != nullptr && !aligned_to(offs, 4)) return MXQ_EALIGN;
+  if (M == 0 || N == 0) return MXQ_OK;
+  const uint64_t scratch_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) / 32;
+  if (scratch_bytes > MXQ_NOALLOC_SCRATCH_BYTES) return MXQ_ESCRATCH;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXQ_ECUDA;
+  uint8_t* ws = noalloc_scratch(dev);
+  if (ws == nullptr) return MXQ_ECUDA;
+  // The 32x1 pass rewrites every byte of the scratch prefix that the swizzle
+  // reads, so nothing left by an earlier call needs clearing.
+  return mxq_quantize_2d_dual_3pass(x, M, N, offs, G, q_row, s_row, q_col, s_col, ws,
+                                    static_cast<int64_t>(scratch_bytes), stream);
 }
