@@ -87,6 +87,11 @@ def _lib():
         lib.oracle_mxfp8_32x1.argtypes = [p, i64, i64, p, p]
         lib.oracle_swizzle_kgroups.restype = ctypes.c_int
         lib.oracle_swizzle_kgroups.argtypes = [p, i64, i64, p, ctypes.c_int32, p]
+        lib.oracle_mx_pack.restype = ctypes.c_int
+        lib.oracle_mx_pack.argtypes = [p, ctypes.c_int, i64, i64, i64, ctypes.c_int, ctypes.c_int, p]
+        lib.oracle_mx_unpack.restype = ctypes.c_int
+        lib.oracle_mx_unpack.argtypes = [p, ctypes.c_int, p, ctypes.c_int, i64, i64, i64,
+                                         ctypes.c_int]
         lib.oracle_rounding_is_nearest_even.restype = ctypes.c_int
         lib.oracle_rounding_is_nearest_even.argtypes = []
         if not lib.oracle_rounding_is_nearest_even():
@@ -271,3 +276,48 @@ def mxfp8_dual_3pass(x_bits: np.ndarray, offs: np.ndarray | None = None) -> dict
     c = mxfp8_32x1(x_bits)
     return {"q_row": r["q_row"], "s_row": r["s_row"], "q_col": c["q_col"],
             "s_col": swizzle_kgroups(c["s_rm"], offs), "s_rm": c["s_rm"].reshape(-1)}
+
+
+# --------------------------------------------------------------------------
+# MX9 / MX6 in the single packed tensor, any axis, strided, padded
+# --------------------------------------------------------------------------
+MX9 = 9
+MX6 = 6
+RECORD_BYTES = {MX9: 18, MX6: 12}
+
+
+def mx_blocks(rows: int, cols: int, axis: int) -> int:
+    lines, length = (rows, cols) if axis == 1 else (cols, rows)
+    return lines * ((length + 15) // 16)
+
+
+def mx_pack(x: np.ndarray, fmt: int, axis: int = 1, cols: int | None = None) -> np.ndarray:
+    """x: [rows, ld] float32 or bf16 bits, of which the first `cols` columns are
+    the tensor (cols defaults to ld).  Returns uint8 [n_blocks, record bytes]."""
+    x = np.ascontiguousarray(x)
+    dt = _dtype_code(x)
+    rows, ld = x.shape
+    cols = ld if cols is None else cols
+    out = np.zeros((mx_blocks(rows, cols, axis), RECORD_BYTES[fmt]), np.uint8)
+    rc = _lib().oracle_mx_pack(_ptr(x), dt, rows, cols, ld, axis, fmt, _ptr(out))
+    if rc != OK:
+        raise OracleError(rc)
+    return out
+
+
+def mx_unpack(packed: np.ndarray, fmt: int, rows: int, cols: int, out_dtype: str,
+              axis: int = 1, ld: int | None = None, fill=None) -> np.ndarray:
+    """Rebuild [rows, ld] (ld defaults to cols); elements outside the tensor
+    keep `fill` (a prefilled array) or zero."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    ld = cols if ld is None else ld
+    if out_dtype == "f32":
+        dt = F32
+        y = np.zeros((rows, ld), np.float32) if fill is None else fill.copy()
+    else:
+        dt = BF16
+        y = np.zeros((rows, ld), np.uint16) if fill is None else fill.copy()
+    rc = _lib().oracle_mx_unpack(_ptr(packed), fmt, _ptr(y), dt, rows, cols, ld, axis)
+    if rc != OK:
+        raise OracleError(rc)
+    return y

@@ -495,5 +495,151 @@ int oracle_mx9_unpack(const int8_t *q, const uint8_t *max_exp,
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------- */
+/* MX9 and MX6 in the single packed tensor, blocked along either axis of a    */
+/* strided 2-D tensor, with a zero-padded partial last block ([MX9] review:   */
+/* "pack mx9 into a single uint8 tensor and dispatch mx6/mx9 to the packed     */
+/* kernels", "consume strided quantization inputs", the axis and padding      */
+/* tests of the suite; the exponent byte is stored at the block record's      */
+/* start).                                                                     */
+/*                                                                             */
+/* READINGS: a record is [exponent byte, prime byte, data]; MX9 data is the    */
+/* 16 int8 q; MX6 uses the same rule with 4 magnitude bits (offset 3 instead   */
+/* of 6, clamp +-15) and stores sixteen 5-bit two's-complement codes, element  */
+/* i at bits 5i..5i+4 of the 10 data bytes read as one little-endian number.   */
+/* Blocks run along `axis` (1: along a row, 0: down a column); the element    */
+/* (r, c) is at x[r * ld + c].  Block order: axis 1 -> b = r * ceil(cols/16) + */
+/* j; axis 0 -> b = c * ceil(rows/16) + j, i.e. blocks of the tensor with the  */
+/* blocked axis moved last.  A partial last block is padded with zeros and     */
+/* then follows the normal rule; unpack writes only real elements.             */
+/* ------------------------------------------------------------------------- */
+
+#define ORC_FMT_MX9 9
+#define ORC_FMT_MX6 6
+
+static int mx_record_bytes(int fmt) { return fmt == ORC_FMT_MX9 ? 18 : 12; }
+
+/* the block rule of oracle_mx9_pack with a format-dependent offset and clamp */
+static void mx_block(const double *v, const int *t, int fmt, uint8_t *e_out, uint8_t *p_out,
+                     int *q) {
+    int E = -127, p, i, d = fmt == ORC_FMT_MX9 ? 6 : 3, qmax = fmt == ORC_FMT_MX9 ? 127 : 15;
+    uint8_t bits = 0;
+    for (i = 0; i < 16; ++i)
+        if (t[i] > E) E = t[i];
+    *e_out = (uint8_t)(E + 127);
+    for (p = 0; p < 8; ++p) {
+        int tp = t[2 * p] > t[2 * p + 1] ? t[2 * p] : t[2 * p + 1];
+        int tau = tp < E;
+        int k = E - d - tau;
+        if (k < -126) k = -126;
+        bits |= (uint8_t)(tau << p);
+        for (i = 2 * p; i < 2 * p + 2; ++i) {
+            double r;
+            if (isnan(v[i])) {
+                q[i] = 0;
+                continue;
+            }
+            r = nearbyint(ldexp(v[i], -k));
+            if (r > qmax) r = qmax;
+            if (r < -qmax) r = -qmax;
+            q[i] = (int)r;
+        }
+    }
+    *p_out = bits;
+}
+
+static int64_t mx_blocks_per_line(int64_t len) { return (len + 15) / 16; }
+
+int oracle_mx_pack(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld, int axis,
+                   int fmt, uint8_t *packed) {
+    int64_t lines, line_len, nbl, b;
+    int RB = mx_record_bytes(fmt);
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EBADDTYPE;
+    if (fmt != ORC_FMT_MX9 && fmt != ORC_FMT_MX6) return ORC_EBADDTYPE;
+    if (rows < 0 || cols < 0 || ld < cols || (axis != 0 && axis != 1)) return ORC_EBADSHAPE;
+    lines = axis == 1 ? rows : cols;
+    line_len = axis == 1 ? cols : rows;
+    nbl = mx_blocks_per_line(line_len);
+    for (b = 0; b < lines * nbl; ++b) {
+        int64_t line = b / nbl, j = b % nbl;
+        double v[16];
+        int t[16], q[16], i;
+        uint8_t *rec = packed + b * RB;
+        for (i = 0; i < 16; ++i) {
+            int64_t pos = 16 * j + i;
+            if (pos >= line_len) { /* zero padding */
+                v[i] = 0.0;
+                t[i] = -127;
+            } else {
+                int64_t idx = axis == 1 ? line * ld + pos : pos * ld + line;
+                v[i] = mx9_value(x, dtype, idx);
+                t[i] = mx9_t(x, dtype, idx);
+            }
+        }
+        mx_block(v, t, fmt, &rec[0], &rec[1], q);
+        if (fmt == ORC_FMT_MX9) {
+            for (i = 0; i < 16; ++i) rec[2 + i] = (uint8_t)(int8_t)q[i];
+        } else {
+            for (i = 0; i < 10; ++i) rec[2 + i] = 0;
+            for (i = 0; i < 16; ++i) {
+                unsigned code = (unsigned)q[i] & 0x1Fu; /* 5-bit two's complement */
+                int bit;
+                for (bit = 0; bit < 5; ++bit)
+                    if (code & (1u << bit)) {
+                        int pos = 5 * i + bit;
+                        rec[2 + pos / 8] |= (uint8_t)(1u << (pos % 8));
+                    }
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+int oracle_mx_unpack(const uint8_t *packed, int fmt, void *y, int dtype, int64_t rows,
+                     int64_t cols, int64_t ld, int axis) {
+    int64_t lines, line_len, nbl, b;
+    int RB = mx_record_bytes(fmt), d = fmt == ORC_FMT_MX9 ? 6 : 3;
+    if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EBADDTYPE;
+    if (fmt != ORC_FMT_MX9 && fmt != ORC_FMT_MX6) return ORC_EBADDTYPE;
+    if (rows < 0 || cols < 0 || ld < cols || (axis != 0 && axis != 1)) return ORC_EBADSHAPE;
+    lines = axis == 1 ? rows : cols;
+    line_len = axis == 1 ? cols : rows;
+    nbl = mx_blocks_per_line(line_len);
+    for (b = 0; b < lines * nbl; ++b) {
+        int64_t line = b / nbl, j = b % nbl;
+        const uint8_t *rec = packed + b * RB;
+        int E = (int)rec[0] - 127, i;
+        for (i = 0; i < 16; ++i) {
+            int64_t pos = 16 * j + i, idx;
+            int tau = (rec[1] >> (i / 2)) & 1, q, k;
+            double v;
+            if (pos >= line_len) continue;
+            if (fmt == ORC_FMT_MX9) {
+                q = (int8_t)rec[2 + i];
+            } else {
+                unsigned code = 0;
+                int bit;
+                for (bit = 0; bit < 5; ++bit) {
+                    int p = 5 * i + bit;
+                    code |= (unsigned)((rec[2 + p / 8] >> (p % 8)) & 1u) << bit;
+                }
+                q = code >= 16 ? (int)code - 32 : (int)code;
+            }
+            k = E - d - tau;
+            if (k < -126) k = -126;
+            v = ldexp((double)q, k);
+            if (fabs(v) >= ldexp(1.0, 128)) v = v > 0 ? INFINITY : -INFINITY;
+            idx = axis == 1 ? line * ld + pos : pos * ld + line;
+            if (dtype == ORC_F32) {
+                float f = (float)v;
+                memcpy((uint32_t *)y + idx, &f, sizeof f);
+            } else {
+                ((uint16_t *)y)[idx] = double_to_bf16_bits(v);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
 /* Rounding-mode guard: the oracle relies on round-to-nearest-even. */
 int oracle_rounding_is_nearest_even(void) { return fegetround() == FE_TONEAREST; }
