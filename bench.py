@@ -482,6 +482,16 @@ def run_sweep(mxq, torch, dev, rank):
                                      bpe * M * N)
             res[f"mx9_unpack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx9_unpack(
                 q, e, p, tdt, (M, N), out=yy, stream=s)), bpe * M * N)
+            # the single packed tensor (MX9 18-byte and MX6 12-byte records, blocks along rows)
+            esz = 4 if dt == "f32" else 2
+            for fmt, name in ((mxq.FMT_MX9, "mx9"), (mxq.FMT_MX6, "mx6")):
+                rec = mxq.mx_pack_packed(xm, fmt, 1)
+                pbytes = (esz + mxq.RECORD_BYTES[fmt] / 16) * M * N
+                res[f"{name}_packed_pack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx_pack_packed(
+                    xm, fmt, 1, out=rec, stream=s)), pbytes)
+                res[f"{name}_packed_unpack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx_unpack_packed(
+                    rec, fmt, yy, 1, stream=s)), pbytes)
+                del rec
             del xm, q, e, p, yy
         if rank == 0:
             line = {"sweep_shape": [M, N], "peak_gbs": peak, "peak_kind": kind,

@@ -134,6 +134,36 @@ int mx9_unpack(const int8_t *q, const uint8_t *max_exp, const uint8_t *prime, vo
                int64_t rows, int64_t cols, cudaStream_t stream);
 
 /*
+ * MX9 and MX6 in one packed uint8 tensor ([MX9] commits "pack mx9 into a
+ * single uint8 tensor and dispatch mx6/mx9 to the packed kernels" and
+ * "consume strided quantization inputs"; the suite's axis, non-contiguous and
+ * padding tests).  One record per 16-element block, [exponent byte, prime
+ * byte, data] (the review excerpt stores the exponent at the record start):
+ *   MXQ_FMT_MX9: data = 16 int8 q as in mx9_pack; 18-byte records, 9 bits/elem.
+ *   MXQ_FMT_MX6: the same rule with 4 magnitude bits, k = max(E - 3 - prime,
+ *     -126), q clamped to [-15, 15], stored as sixteen 5-bit two's-complement
+ *     codes (element i at bits 5i..5i+4 of the 10 data bytes read as one
+ *     little-endian number); 12-byte records, 6 bits/elem.
+ * The 2-D tensor has `rows` x `cols` elements, element (r, c) at x[r*ld + c]
+ * (ld >= cols, any element-aligned x: strided views are accepted).  Blocks
+ * run along `axis`: 1 = along each row, block b = r*ceil(cols/16) + j over
+ * columns 16j..16j+15; 0 = down each column, b = c*ceil(rows/16) + j over rows
+ * 16j..16j+15 (the tensor with the blocked axis moved last).  A partial last
+ * block is zero-padded and then follows the normal rule; unpack writes only
+ * the tensor's own elements.  packed: n_blocks * record bytes, 2-byte (MX9) or
+ * 4-byte (MX6) aligned (16-byte alignment is faster).  Shape and axis are not
+ * stored: the caller passes them back to unpack.
+ */
+#define MXQ_FMT_MX9 9
+#define MXQ_FMT_MX6 6
+#define MXQ_MX9_RECORD_BYTES 18
+#define MXQ_MX6_RECORD_BYTES 12
+int mx_pack_packed(const void *x, int dtype, int64_t rows, int64_t cols, int64_t ld, int axis,
+                   int fmt, uint8_t *packed, cudaStream_t stream);
+int mx_unpack_packed(const uint8_t *packed, int fmt, void *y, int dtype, int64_t rows,
+                     int64_t cols, int64_t ld, int axis, cudaStream_t stream);
+
+/*
  * The three-pass composition that the fused cast replaces ([AO] description,
  * first paragraph: a 1x32 cast along N, a 32x1 cast along M and a standalone
  * K-groups swizzle of the colwise scales, reading x twice).  Kept so that the

@@ -37,6 +37,9 @@ ENULL = -7
 F32 = 0
 BF16 = 1
 MAX_GROUPS = 1024
+FMT_MX9 = 9
+FMT_MX6 = 6
+RECORD_BYTES = {FMT_MX9: 18, FMT_MX6: 12}
 DEV_BADOFFS = 0x1
 DEV_TIMEOUT = 0x2
 
@@ -75,6 +78,12 @@ def lib() -> ctypes.CDLL:
         L.mxq_swizzle_kgroups.argtypes = [vp, i64, i64, vp, i32, vp, vp]
         L.mxq_quantize_2d_dual_3pass.restype = ctypes.c_int
         L.mxq_quantize_2d_dual_3pass.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp, i64, vp]
+        L.mx_pack_packed.restype = ctypes.c_int
+        L.mx_pack_packed.argtypes = [vp, ctypes.c_int, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                     vp, vp]
+        L.mx_unpack_packed.restype = ctypes.c_int
+        L.mx_unpack_packed.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i64, i64, i64,
+                                       ctypes.c_int, vp]
         L.mxq_device_status.restype = ctypes.c_int
         L.mxq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.mxq_status_string.restype = ctypes.c_char_p
@@ -350,4 +359,66 @@ def mx9_unpack(q, max_exp, prime, out_dtype, shape, *, out=None, stream=None):
                               dt, rows, cols, _stream_handle(q.device, stream))
     if rc != OK:
         raise MxqError(rc, "mx9_unpack")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# MX9 / MX6 in one packed tensor, any axis, strided views, padded blocks
+# ---------------------------------------------------------------------------
+
+def _view_2d(t, name):
+    """(rows, cols, ld) of a 2-D CUDA tensor whose rows may be strided."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+    if t.dim() != 2 or t.stride(1) != 1 or (t.shape[0] > 1 and t.stride(0) < t.shape[1]):
+        raise ValueError(f"{name} must be 2-D with unit column stride")
+    rows, cols = t.shape
+    return rows, cols, (t.stride(0) if rows > 1 else cols)
+
+
+def mx_blocks(rows: int, cols: int, axis: int) -> int:
+    lines, length = (rows, cols) if axis == 1 else (cols, rows)
+    return lines * ((length + 15) // 16)
+
+
+def mx_pack_packed(x, fmt: int = FMT_MX9, axis: int = 1, *, out=None, stream=None):
+    """Pack a fp32/bf16 CUDA tensor (strided rows allowed) into uint8 records
+    [n_blocks, 18 (MX9) or 12 (MX6)], blocks of 16 along `axis`."""
+    torch = _torch()
+    if fmt not in RECORD_BYTES:
+        raise ValueError(f"unknown MX format {fmt} (FMT_MX9 or FMT_MX6)")
+    dt = _dtype_code(x)
+    rows, cols, ld = _view_2d(x, "x")
+    nb = mx_blocks(rows, cols, axis)
+    if out is None:
+        out = torch.empty((nb, RECORD_BYTES[fmt]), dtype=torch.uint8, device=x.device)
+    _check_cuda(out, "out")
+    if out.dtype != torch.uint8 or out.numel() != nb * RECORD_BYTES[fmt] or out.device != x.device:
+        raise ValueError("out must be uint8 [n_blocks, record bytes] on x's device")
+    with torch.cuda.device(x.device):
+        rc = lib().mx_pack_packed(ctypes.c_void_p(x.data_ptr()), dt, rows, cols, ld, axis, fmt,
+                                  ctypes.c_void_p(out.data_ptr()), _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mx_pack_packed")
+    return out
+
+
+def mx_unpack_packed(packed, fmt: int, out, axis: int = 1, *, stream=None):
+    """Rebuild into `out` (a fp32/bf16 CUDA tensor, strided rows allowed) from
+    records produced by mx_pack_packed with the same shape and axis."""
+    torch = _torch()
+    if fmt not in RECORD_BYTES:
+        raise ValueError(f"unknown MX format {fmt} (FMT_MX9 or FMT_MX6)")
+    dt = _dtype_code(out)
+    rows, cols, ld = _view_2d(out, "out")
+    _check_cuda(packed, "packed")
+    nb = mx_blocks(rows, cols, axis)
+    if packed.dtype != torch.uint8 or packed.numel() != nb * RECORD_BYTES[fmt]:
+        raise ValueError("packed must be uint8 [n_blocks, record bytes] for this shape")
+    with torch.cuda.device(out.device):
+        rc = lib().mx_unpack_packed(ctypes.c_void_p(packed.data_ptr()), fmt,
+                                    ctypes.c_void_p(out.data_ptr()), dt, rows, cols, ld, axis,
+                                    _stream_handle(out.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mx_unpack_packed")
     return out

@@ -1,0 +1,466 @@
+// mx_packed.cu -- MX9 and MX6 in one packed tensor, blocked along either axis
+// of a strided 2-D tensor, with a zero-padded partial last block.
+//
+// AMD-AGI/ALTO PR #33 "mx9: add fused MX9 quantization kernel with
+// pack/unpack": the later commits pack MX9 "into a single uint8 tensor",
+// dispatch MX6 and MX9 to the packed kernels, "consume strided quantization
+// inputs"; the suite covers blocking along an axis, non-contiguous input and
+// padding.  One record per 16-element block: [exponent byte, prime byte,
+// data], the exponent byte first as in the review excerpt.  MX9 data: the 16
+// int8 q (k = max(E - 6 - prime, -126), clamp +-127).  MX6 data: the same rule
+// with 4 magnitude bits (k = max(E - 3 - prime, -126), clamp +-15), sixteen
+// 5-bit two's-complement codes, element i at bits 5i..5i+4 of the 10 data
+// bytes read as one little-endian number.
+//
+// One thread owns one block.  Along axis 1 (a row) a warp's 32 blocks are
+// consecutive records: the warp stages them in shared memory and moves them
+// with 16-byte coalesced copies; along axis 0 (a column) the lanes of a warp
+// take neighbouring columns, so every element load and store is coalesced and
+// each record is written with its own narrow stores.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mxq.h"
+#include "mxq_device.cuh"
+#include "mxq_host.h"
+
+namespace {
+
+using namespace mxq;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxRecord = MXQ_MX9_RECORD_BYTES;
+
+template <int kFmt>
+struct Fmt {
+  static constexpr int kRecord = kFmt == MXQ_FMT_MX9 ? MXQ_MX9_RECORD_BYTES : MXQ_MX6_RECORD_BYTES;
+  static constexpr int kOffset = kFmt == MXQ_FMT_MX9 ? 6 : 3;    // E - k for a non-demoted pair
+  static constexpr int kQMax = kFmt == MXQ_FMT_MX9 ? 127 : 15;   // symmetric clamp
+};
+
+struct Geometry {
+  int64_t rows, cols, ld;
+  int axis;
+  __host__ __device__ int64_t lines() const { return axis == 1 ? rows : cols; }
+  __host__ __device__ int64_t len() const { return axis == 1 ? cols : rows; }
+};
+
+__device__ __forceinline__ int64_t elem_index(const Geometry& g, int64_t line, int64_t pos) {
+  return g.axis == 1 ? line * g.ld + pos : pos * g.ld + line;
+}
+
+// Work item w -> (line, j): along axis 1 consecutive work items are
+// consecutive blocks of a row; along axis 0 consecutive work items are the
+// same block position j of neighbouring columns.
+__device__ __forceinline__ void work_to_block(const Geometry& g, int64_t nbl, int64_t w,
+                                              int64_t* line, int64_t* j) {
+  if (g.axis == 1) {
+    *line = w / nbl;
+    *j = w - *line * nbl;
+  } else {
+    const int64_t lines = g.lines();
+    *j = w / lines;
+    *line = w - *j * lines;
+  }
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t load_bits(const uint8_t* x, int64_t idx) {
+  if (kBF16) return static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(x) + idx)) << 16;
+  return __ldg(reinterpret_cast<const uint32_t*>(x) + idx);
+}
+
+// 2^-k for a pair: k = max(E - off - t, -126) with E = eb8 - 127, so
+// 127 - k = min(254 - eb8 + off + t, 253) (always a normal exponent field).
+template <int kOff>
+__device__ __forceinline__ float pair_mult(uint32_t eb8, uint32_t t) {
+  return __uint_as_float(min(254u + kOff - eb8 + t, 253u) << 23);
+}
+
+template <int kQMax>
+__device__ __forceinline__ int q_of(float x, float m) {
+  const int r = __float2int_rn(fmul_rn_noftz(x, m));  // NaN -> 0, +-Inf saturate
+  return max(-kQMax, min(kQMax, r));
+}
+
+// The block rule on 16 fp32 bit patterns (zero for padding): exponent byte,
+// prime byte and the 16 integer values.
+template <int kFmt>
+__device__ __forceinline__ void block_rule(const uint32_t* f, uint32_t* eb8_out, uint32_t* bits_out,
+                                           int* q) {
+  uint32_t pe[8], eb = 0;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    pe[p] = max(f[2 * p] & 0x7F800000u, f[2 * p + 1] & 0x7F800000u);
+    eb = max(eb, pe[p]);
+  }
+  const uint32_t eb8 = eb >> 23;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t t = pe[p] < eb;
+    bits |= t << p;
+    const float m = pair_mult<Fmt<kFmt>::kOffset>(eb8, t);
+    q[2 * p] = q_of<Fmt<kFmt>::kQMax>(__uint_as_float(f[2 * p]), m);
+    q[2 * p + 1] = q_of<Fmt<kFmt>::kQMax>(__uint_as_float(f[2 * p + 1]), m);
+  }
+  *eb8_out = eb8;
+  *bits_out = bits;
+}
+
+// Record bytes as 32-bit words (the MX9 record's last word holds 2 bytes).
+template <int kFmt>
+__device__ __forceinline__ void encode_record(uint32_t eb8, uint32_t bits, const int* q,
+                                              uint32_t* w) {
+  const uint32_t head = eb8 | (bits << 8);
+  if (kFmt == MXQ_FMT_MX9) {
+    uint32_t b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) b[i] = static_cast<uint32_t>(q[i]) & 0xFFu;
+    w[0] = head | (b[0] << 16) | (b[1] << 24);
+#pragma unroll
+    for (int k = 1; k < 4; ++k)
+      w[k] = b[4 * k - 2] | (b[4 * k - 1] << 8) | (b[4 * k] << 16) | (b[4 * k + 1] << 24);
+    w[4] = b[14] | (b[15] << 8);
+  } else {
+    uint64_t lo = 0;
+    uint32_t hi = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint64_t code = static_cast<uint64_t>(static_cast<uint32_t>(q[i]) & 0x1Fu);
+      const int s = 5 * i;
+      if (s + 5 <= 64) {
+        lo |= code << s;
+      } else if (s >= 64) {
+        hi |= static_cast<uint32_t>(code << (s - 64));
+      } else {
+        lo |= code << s;
+        hi |= static_cast<uint32_t>(code >> (64 - s));
+      }
+    }
+    w[0] = head | (static_cast<uint32_t>(lo & 0xFFFFu) << 16);
+    w[1] = static_cast<uint32_t>(lo >> 16);
+    w[2] = static_cast<uint32_t>(lo >> 48) | (hi << 16);
+  }
+}
+
+template <int kFmt>
+__device__ __forceinline__ void decode_record(const uint32_t* w, uint32_t* eb8, uint32_t* bits,
+                                              int* q) {
+  *eb8 = w[0] & 0xFFu;
+  *bits = (w[0] >> 8) & 0xFFu;
+  if (kFmt == MXQ_FMT_MX9) {
+    q[0] = static_cast<int8_t>((w[0] >> 16) & 0xFF);
+    q[1] = static_cast<int8_t>(w[0] >> 24);
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+      q[4 * k - 2] = static_cast<int8_t>(w[k] & 0xFF);
+      q[4 * k - 1] = static_cast<int8_t>((w[k] >> 8) & 0xFF);
+      q[4 * k] = static_cast<int8_t>((w[k] >> 16) & 0xFF);
+      q[4 * k + 1] = static_cast<int8_t>(w[k] >> 24);
+    }
+    q[14] = static_cast<int8_t>(w[4] & 0xFF);
+    q[15] = static_cast<int8_t>((w[4] >> 8) & 0xFF);
+  } else {
+    const uint64_t lo = static_cast<uint64_t>(w[0] >> 16) | (static_cast<uint64_t>(w[1]) << 16) |
+                        (static_cast<uint64_t>(w[2] & 0xFFFFu) << 48);
+    const uint32_t hi = w[2] >> 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int s = 5 * i;
+      uint32_t code;
+      if (s + 5 <= 64)
+        code = static_cast<uint32_t>(lo >> s) & 0x1Fu;
+      else if (s >= 64)
+        code = (hi >> (s - 64)) & 0x1Fu;
+      else
+        code = (static_cast<uint32_t>(lo >> s) | (hi << (64 - s))) & 0x1Fu;
+      q[i] = code >= 16 ? static_cast<int>(code) - 32 : static_cast<int>(code);
+    }
+  }
+}
+
+template <int kFmt>
+__device__ __forceinline__ void store_record_narrow(uint8_t* dst, const uint32_t* w) {
+  if (kFmt == MXQ_FMT_MX9) {  // 18 bytes, 2-byte aligned
+    uint16_t* h = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      h[2 * k] = static_cast<uint16_t>(w[k] & 0xFFFFu);
+      h[2 * k + 1] = static_cast<uint16_t>(w[k] >> 16);
+    }
+    h[8] = static_cast<uint16_t>(w[4] & 0xFFFFu);
+  } else {  // 12 bytes, 4-byte aligned
+    uint32_t* p = reinterpret_cast<uint32_t*>(dst);
+    p[0] = w[0];
+    p[1] = w[1];
+    p[2] = w[2];
+  }
+}
+
+template <int kFmt>
+__device__ __forceinline__ void load_record_narrow(const uint8_t* src, uint32_t* w) {
+  if (kFmt == MXQ_FMT_MX9) {
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(src);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = static_cast<uint32_t>(__ldg(h + 2 * k)) | (static_cast<uint32_t>(__ldg(h + 2 * k + 1)) << 16);
+    w[4] = __ldg(h + 8);
+  } else {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(src);
+    w[0] = __ldg(p);
+    w[1] = __ldg(p + 1);
+    w[2] = __ldg(p + 2);
+  }
+}
+
+// Copy `bytes` between global and a warp's 16-byte aligned shared staging
+// area (global side 16-byte aligned when `aligned`, else byte by byte).
+__device__ __forceinline__ void warp_copy_out(uint8_t* g, const uint8_t* s, int bytes, bool aligned,
+                                              int lane) {
+  if (aligned) {
+    const int n16 = bytes >> 4;
+    for (int i = lane; i < n16; i += 32)
+      reinterpret_cast<uint4*>(g)[i] = reinterpret_cast<const uint4*>(s)[i];
+    for (int i = (n16 << 4) + lane; i < bytes; i += 32) g[i] = s[i];
+  } else {
+    for (int i = lane; i < bytes; i += 32) g[i] = s[i];
+  }
+}
+
+__device__ __forceinline__ void warp_copy_in(uint8_t* s, const uint8_t* g, int bytes, bool aligned,
+                                             int lane) {
+  if (aligned) {
+    const int n16 = bytes >> 4;
+    for (int i = lane; i < n16; i += 32)
+      reinterpret_cast<uint4*>(s)[i] = __ldg(reinterpret_cast<const uint4*>(g) + i);
+    for (int i = (n16 << 4) + lane; i < bytes; i += 32) s[i] = __ldg(g + i);
+  } else {
+    for (int i = lane; i < bytes; i += 32) s[i] = __ldg(g + i);
+  }
+}
+
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_pack_packed_kernel(const uint8_t* __restrict__ x, Geometry g, bool vec_rows,
+                          bool packed_aligned, uint8_t* __restrict__ packed) {
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nbl = (g.len() + 15) / 16;
+  const int64_t nb = g.lines() * nbl;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kThreads + warp * 32; w0 < nb; w0 += stride) {
+    const int64_t w = w0 + lane;  // warp-uniform loop; lanes past nb idle
+    uint32_t rec[5] = {0, 0, 0, 0, 0};
+    int64_t b = 0;
+    if (w < nb) {
+      int64_t line, j;
+      work_to_block(g, nbl, w, &line, &j);
+      b = line * nbl + j;
+      const int64_t valid = min(static_cast<int64_t>(16), g.len() - 16 * j);
+      uint32_t f[16];
+      if (g.axis == 1 && vec_rows && valid == 16) {
+        const uint8_t* src = x + elem_index(g, line, 16 * j) * (kBF16 ? 2 : 4);
+        if (kBF16) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + k);
+            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              f[8 * k + 2 * i] = wd[i] << 16;
+              f[8 * k + 2 * i + 1] = wd[i] & 0xFFFF0000u;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + k);
+            f[4 * k] = v.x;
+            f[4 * k + 1] = v.y;
+            f[4 * k + 2] = v.z;
+            f[4 * k + 3] = v.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          f[i] = i < valid ? load_bits<kBF16>(x, elem_index(g, line, 16 * j + i)) : 0u;
+      }
+      uint32_t eb8, bits;
+      int q[16];
+      block_rule<kFmt>(f, &eb8, &bits, q);
+      encode_record<kFmt>(eb8, bits, q, rec);
+    }
+    if (g.axis == 1) {
+      // the warp's records b = w0 .. w0+31 are contiguous: stage and copy out
+      uint8_t* st = stage[warp];
+      if (w < nb) {
+        uint16_t* h = reinterpret_cast<uint16_t*>(st + lane * RB);
+#pragma unroll
+        for (int k = 0; k < (RB + 3) / 4; ++k) {
+          h[2 * k] = static_cast<uint16_t>(rec[k] & 0xFFFFu);
+          if (4 * k + 2 < RB) h[2 * k + 1] = static_cast<uint16_t>(rec[k] >> 16);
+        }
+      }
+      __syncwarp();
+      const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
+      warp_copy_out(packed + w0 * RB, st, static_cast<int>(nvalid) * RB, packed_aligned, lane);
+      __syncwarp();
+    } else if (w < nb) {
+      store_record_narrow<kFmt>(packed + b * RB, rec);
+    }
+  }
+}
+
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_unpack_packed_kernel(const uint8_t* __restrict__ packed, Geometry g, bool vec_rows,
+                            bool packed_aligned, uint8_t* __restrict__ y) {
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nbl = (g.len() + 15) / 16;
+  const int64_t nb = g.lines() * nbl;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kThreads + warp * 32; w0 < nb; w0 += stride) {
+    const int64_t w = w0 + lane;
+    uint32_t rec[5] = {0, 0, 0, 0, 0};
+    if (g.axis == 1) {
+      uint8_t* st = stage[warp];
+      const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
+      warp_copy_in(st, packed + w0 * RB, static_cast<int>(nvalid) * RB, packed_aligned, lane);
+      __syncwarp();
+      if (w < nb) {
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(st + lane * RB);
+#pragma unroll
+        for (int k = 0; k < (RB + 3) / 4; ++k)
+          rec[k] = static_cast<uint32_t>(h[2 * k]) |
+                   (4 * k + 2 < RB ? static_cast<uint32_t>(h[2 * k + 1]) << 16 : 0u);
+      }
+      __syncwarp();
+    }
+    if (w >= nb) continue;
+    int64_t line, j;
+    work_to_block(g, nbl, w, &line, &j);
+    const int64_t b = line * nbl + j;
+    if (g.axis != 1) load_record_narrow<kFmt>(packed + b * RB, rec);
+    uint32_t eb8, bits;
+    int q[16];
+    decode_record<kFmt>(rec, &eb8, &bits, q);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t t = (bits >> (i / 2)) & 1u;
+      // 2^k, k = max(E - off - t, -126): exponent field min(eb8 - off - t, 127 - 126)
+      const int kf = max(static_cast<int>(eb8) - Fmt<kFmt>::kOffset - static_cast<int>(t), 1);
+      v[i] = fmul_rn_noftz(static_cast<float>(q[i]), __uint_as_float(static_cast<uint32_t>(kf) << 23));
+    }
+    const int64_t valid = min(static_cast<int64_t>(16), g.len() - 16 * j);
+    if (g.axis == 1 && vec_rows && valid == 16) {
+      uint8_t* dst = y + elem_index(g, line, 16 * j) * (kBF16 ? 2 : 4);
+      if (kBF16) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          uint32_t wd[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            wd[i] = (__float_as_uint(v[8 * k + 2 * i]) >> 16) |
+                    (__float_as_uint(v[8 * k + 2 * i + 1]) & 0xFFFF0000u);
+          reinterpret_cast<uint4*>(dst)[k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          reinterpret_cast<float4*>(dst)[k] =
+              make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i >= valid) break;
+        const int64_t idx = elem_index(g, line, 16 * j + i);
+        if (kBF16)
+          reinterpret_cast<uint16_t*>(y)[idx] = static_cast<uint16_t>(__float_as_uint(v[i]) >> 16);
+        else
+          reinterpret_cast<float*>(y)[idx] = v[i];
+      }
+    }
+  }
+}
+
+int check_args(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, int axis, int fmt,
+               const void* packed, int64_t* nb_out) {
+  if (dtype != MXQ_F32 && dtype != MXQ_BF16) return MXQ_EBADDTYPE;
+  if (fmt != MXQ_FMT_MX9 && fmt != MXQ_FMT_MX6) return MXQ_EBADDTYPE;
+  if (rows < 0 || cols < 0 || ld < cols || (axis != 0 && axis != 1)) return MXQ_EBADSHAPE;
+  if (rows > 0 && ld > 0 && rows > (INT64_MAX / 8) / ld) return MXQ_EBADSHAPE;
+  const int64_t lines = axis == 1 ? rows : cols, len = axis == 1 ? cols : rows;
+  *nb_out = lines * ((len + 15) / 16);
+  if (*nb_out == 0) return MXQ_OK;
+  if (!x || !packed) return MXQ_ENULL;
+  const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
+  if (!aligned_to(x, esize)) return MXQ_EALIGN;
+  if (!aligned_to(packed, fmt == MXQ_FMT_MX9 ? 2 : 4)) return MXQ_EALIGN;
+  const int RB = fmt == MXQ_FMT_MX9 ? MXQ_MX9_RECORD_BYTES : MXQ_MX6_RECORD_BYTES;
+  const ByteRange r[2] = {
+      {reinterpret_cast<uintptr_t>(x), esize * static_cast<uint64_t>((rows - 1) * ld + cols)},
+      {reinterpret_cast<uintptr_t>(packed), static_cast<uint64_t>(*nb_out) * RB}};
+  if (ranges_overlap(r, 2)) return MXQ_EOVERLAP;
+  return MXQ_OK;
+}
+
+template <typename Kernel, typename... Args>
+int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
+  const int sms = sm_count_current_device(nullptr);
+  if (sms <= 0) return MXQ_ECUDA;
+  const int64_t want = (nb + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kThreads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
+}
+
+}  // namespace
+
+extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                              int axis, int fmt, uint8_t* packed, cudaStream_t stream) {
+  int64_t nb = 0;
+  const int rc = check_args(x, dtype, rows, cols, ld, axis, fmt, packed, &nb);
+  if (rc != MXQ_OK || nb == 0) return rc;
+  const Geometry g{rows, cols, ld, axis};
+  const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
+  const bool vec_rows = aligned_to(x, 16) && (ld * esize) % 16 == 0;
+  const bool pal = aligned_to(packed, 16);
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  if (dtype == MXQ_F32)
+    return fmt == MXQ_FMT_MX9
+               ? launch(mx_pack_packed_kernel<false, MXQ_FMT_MX9>, nb, stream, xb, g, vec_rows, pal, packed)
+               : launch(mx_pack_packed_kernel<false, MXQ_FMT_MX6>, nb, stream, xb, g, vec_rows, pal, packed);
+  return fmt == MXQ_FMT_MX9
+             ? launch(mx_pack_packed_kernel<true, MXQ_FMT_MX9>, nb, stream, xb, g, vec_rows, pal, packed)
+             : launch(mx_pack_packed_kernel<true, MXQ_FMT_MX6>, nb, stream, xb, g, vec_rows, pal, packed);
+}
+
+extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dtype, int64_t rows,
+                                int64_t cols, int64_t ld, int axis, cudaStream_t stream) {
+  int64_t nb = 0;
+  const int rc = check_args(y, dtype, rows, cols, ld, axis, fmt, packed, &nb);
+  if (rc != MXQ_OK || nb == 0) return rc;
+  const Geometry g{rows, cols, ld, axis};
+  const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
+  const bool vec_rows = aligned_to(y, 16) && (ld * esize) % 16 == 0;
+  const bool pal = aligned_to(packed, 16);
+  uint8_t* yb = static_cast<uint8_t*>(y);
+  if (dtype == MXQ_F32)
+    return fmt == MXQ_FMT_MX9
+               ? launch(mx_unpack_packed_kernel<false, MXQ_FMT_MX9>, nb, stream, packed, g, vec_rows, pal, yb)
+               : launch(mx_unpack_packed_kernel<false, MXQ_FMT_MX6>, nb, stream, packed, g, vec_rows, pal, yb);
+  return fmt == MXQ_FMT_MX9
+             ? launch(mx_unpack_packed_kernel<true, MXQ_FMT_MX9>, nb, stream, packed, g, vec_rows, pal, yb)
+             : launch(mx_unpack_packed_kernel<true, MXQ_FMT_MX6>, nb, stream, packed, g, vec_rows, pal, yb);
+}

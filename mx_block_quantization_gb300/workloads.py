@@ -133,9 +133,9 @@ def mx9_outliers(rows: int = 4096, cols: int = 4096, seed: int = SEED,
     n_out = int(round(flat.size * outlier_frac))
     if n_out:
         flat[g.choice(flat.size, size=n_out, replace=False)] *= np.float32(outlier_mult)
-    nb = flat.size // 16
+    nb = flat.size // 16                                            # whole 16-blocks
     blocks = g.choice(nb, size=zero_blocks + tiny_blocks, replace=False)
-    bv = flat.reshape(nb, 16)
+    bv = flat[:nb * 16].reshape(nb, 16)
     bv[blocks[:zero_blocks]] = 0.0
     tiny = g.standard_normal(size=(tiny_blocks, 16)) * 1e-40       # float64, then
     bv[blocks[zero_blocks:]] = tiny.astype(np.float32)              # fp32 subnormals

@@ -155,3 +155,21 @@ def test_composition_rejections(L):
     assert L.mxq_swizzle_kgroups(vp(A), N, M, vp(0), 1, vp(A + MN), None) == mxq.EBADOFFS
     assert L.mxq_swizzle_kgroups(vp(A), N, M, vp(0), 0, vp(A + 16), None) == mxq.EOVERLAP
     assert L.mxq_swizzle_kgroups(vp(A), 0, M, vp(0), 0, vp(0), None) == mxq.OK
+
+
+def test_packed_variant_rejections(L):
+    vp = ctypes.c_void_p
+
+    def pack(x=A, dtype=0, rows=4, cols=32, ld=32, axis=1, fmt=9, out=A + 8192):
+        return L.mx_pack_packed(vp(x), dtype, rows, cols, ld, axis, fmt, vp(out), None)
+    assert pack(fmt=7) == mxq.EBADDTYPE
+    assert pack(dtype=3) == mxq.EBADDTYPE
+    assert pack(ld=16) == mxq.EBADSHAPE
+    assert pack(axis=2) == mxq.EBADSHAPE
+    assert pack(x=0) == mxq.ENULL
+    assert pack(x=A + 2) == mxq.EALIGN          # fp32 elements need 4-byte alignment
+    assert pack(out=A + 1) == mxq.EALIGN        # MX9 records need 2-byte alignment
+    assert pack(out=A + 64) == mxq.EOVERLAP
+    assert pack(rows=0) == mxq.OK
+    assert L.mx_unpack_packed(vp(A), 6, vp(A + 64), 0, 4, 32, 32, 1, None) == mxq.EOVERLAP
+    assert L.mx_unpack_packed(vp(A + 2), 6, vp(A + 4096), 0, 4, 32, 32, 1, None) == mxq.EALIGN

@@ -1,0 +1,98 @@
+"""GPU parity of MX9/MX6 in one packed tensor (mx_pack_packed / mx_unpack_packed)
+against the CPU oracle, byte for byte: both formats, fp32 and bf16, blocks
+along either axis, strided (wider) rows, zero-padded partial blocks."""
+import numpy as np
+import pytest
+import torch
+
+import mx_block_quantization_gb300 as mxq
+import oracle
+from mx_block_quantization_gb300 import workloads as W
+from tests.gpu_util import assert_bytes_equal, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [mxq.FMT_MX9, mxq.FMT_MX6]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+    yield
+    assert mxq.device_status(clear=True) == 0
+
+
+def _dev(a: np.ndarray) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _check(x_full: np.ndarray, cols: int, fmt: int, axis: int, tag: str):
+    """x_full: [rows, ld] host array whose first `cols` columns are the tensor."""
+    rows, ld = x_full.shape
+    xd = _dev(x_full)[:, :cols]                      # a strided view when ld > cols
+    got = mxq.mx_pack_packed(xd, fmt, axis)
+    want = oracle.mx_pack(x_full, fmt, axis=axis, cols=cols)
+    torch.cuda.synchronize()
+    assert_bytes_equal(got.cpu().numpy(), want, f"{tag} pack")
+    # unpack into a prefilled wider buffer: only the tensor's elements change
+    is_bf16 = x_full.dtype == np.uint16
+    fill_val = 0x5A5A if is_bf16 else np.float32(-3.25)
+    fill = np.full((rows, ld), fill_val, x_full.dtype)
+    yd = _dev(fill)
+    mxq.mx_unpack_packed(got, fmt, yd[:, :cols], axis)
+    ref = oracle.mx_unpack(want, fmt, rows, cols, "bf16" if is_bf16 else "f32", axis=axis, ld=ld,
+                           fill=fill)
+    torch.cuda.synchronize()
+    ygot = yd.cpu().view(torch.int16 if is_bf16 else torch.int32).numpy()
+    assert_bytes_equal(ygot.view(np.uint8), ref.view(np.uint8), f"{tag} unpack")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("axis", [0, 1])
+@pytest.mark.parametrize("rows,cols,ld", [(64, 256, 256), (20, 37, 37), (48, 80, 112),
+                                          (33, 16, 24), (1, 15, 15), (257, 129, 136)])
+def test_packed_shapes(fmt, dt, axis, rows, cols, ld):
+    x = np.zeros((rows, ld), np.float32)
+    x[:, :cols] = W.mx9_outliers(rows, cols, seed=rows * cols + axis, zero_blocks=0, tiny_blocks=0)
+    x[:, cols:] = np.float32(9e30)                   # outside the tensor: must not matter
+    if dt == "bf16":
+        x = W.f32_to_bf16_bits(x)
+    _check(x, cols, fmt, axis, f"fmt{fmt} {dt} axis{axis} {rows}x{cols}/{ld}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("axis", [0, 1])
+def test_packed_outlier_workload(fmt, axis):
+    """The [4096, 4096] outlier workload (zero and ~1e-40 blocks included)."""
+    x = W.mx9_outliers()
+    _check(x, 4096, fmt, axis, f"fmt{fmt} axis{axis} 4096^2")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_packed_every_bf16_pattern(fmt):
+    g = np.random.Generator(np.random.PCG64(3))
+    x = g.permutation(np.arange(65536, dtype=np.uint32).astype(np.uint16)).reshape(256, 256)
+    _check(x, 256, fmt, 1, f"fmt{fmt} bf16 patterns")
+    _check(x, 256, fmt, 0, f"fmt{fmt} bf16 patterns axis0")
+
+
+def test_packed_mx9_matches_split_kernel():
+    """The packed MX9 records hold the split kernels' bytes (GPU against GPU)."""
+    x = _dev(W.mx9_outliers(512, 512, seed=5))
+    rec = mxq.mx_pack_packed(x, mxq.FMT_MX9, 1)
+    q, e, p = mxq.mx9_pack(x)
+    torch.cuda.synchronize()
+    r = rec.cpu().numpy()
+    assert np.array_equal(r[:, 0], e.cpu().numpy())
+    assert np.array_equal(r[:, 1], p.cpu().numpy()[:, 0])
+    assert np.array_equal(r[:, 2:].view(np.int8), q.cpu().numpy())
+
+
+def test_packed_rejections():
+    with pytest.raises(ValueError):
+        mxq.mx_pack_packed(torch.zeros((4, 16), device="cuda"), 7, 1)       # unknown format
+    with pytest.raises(ValueError):
+        mxq.mx_pack_packed(torch.zeros((4, 16), device="cuda").t(), mxq.FMT_MX9, 1)
