@@ -232,6 +232,16 @@ int mxq_quantize_2d_dual_3pass_noalloc(const void *x, int64_t M, int64_t N, cons
  */
 int mxq_device_status(uint32_t *out, int clear);
 
+/*
+ * Self-test of failure detection, on the GPU and without a fault: launches one
+ * warp that waits, with the same bounded wait the pipelines use, on an
+ * mbarrier nothing ever completes.  The wait gives up after `limit_ns`
+ * nanoseconds (1e6 .. 4e9, else MXQ_EBADSHAPE), the kernel records
+ * MXQ_DEV_TIMEOUT in the device status word and returns, and the context stays
+ * usable.  The production kernels use a 4 s limit per wait.
+ */
+int mxq_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *mxq_status_string(int status);
 

@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.mx_unpack_packed.restype = ctypes.c_int
         L.mx_unpack_packed.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i64, i64, i64,
                                        ctypes.c_int, vp]
+        L.mxq_selftest_wait_timeout.restype = ctypes.c_int
+        L.mxq_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         L.mxq_device_status.restype = ctypes.c_int
         L.mxq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.mxq_status_string.restype = ctypes.c_char_p
@@ -110,6 +112,16 @@ def device_status(clear: bool = True) -> int:
     if rc != OK:
         raise MxqError(rc, "mxq_device_status")
     return int(out.value)
+
+
+def selftest_wait_timeout(limit_ns: int = 50_000_000, stream=None) -> None:
+    """Launch the bounded-wait self-test (see mxq.h); afterwards device_status()
+    reports DEV_TIMEOUT."""
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = lib().mxq_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(s.cuda_stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------------------

@@ -47,6 +47,9 @@ using namespace mxq;
 #ifndef MXQ_DUAL_GROUP_ROWS
 #define MXQ_DUAL_GROUP_ROWS 8
 #endif
+#ifndef MXQ_DUAL_L2_HINTS  // bit 0: evict-first on the input loads, bit 1: on the data stores
+#define MXQ_DUAL_L2_HINTS 0
+#endif
 constexpr int kTile = 128;
 constexpr int kStages = MXQ_DUAL_STAGES;              // input ring depth (tiles)
 constexpr int kOutBufs = MXQ_DUAL_OUTBUFS;            // staged output tiles
@@ -317,8 +320,14 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
     const uint32_t dst = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
     mbar_arrive_expect_tx(bars.full(s), kInStageBytes);
     const int32_t c0 = static_cast<int32_t>(tj * kTile), r0 = static_cast<int32_t>(ti * kTile);
-    tma_load_2d(dst, &tm_x, c0, r0, bars.full(s));
-    tma_load_2d(dst + kHalfBytes, &tm_x, c0 + 64, r0, bars.full(s));
+    if (MXQ_DUAL_L2_HINTS & 1) {
+      const uint64_t pol = l2_policy_evict_first();
+      tma_load_2d_hint(dst, &tm_x, c0, r0, bars.full(s), pol);
+      tma_load_2d_hint(dst + kHalfBytes, &tm_x, c0 + 64, r0, bars.full(s), pol);
+    } else {
+      tma_load_2d(dst, &tm_x, c0, r0, bars.full(s));
+      tma_load_2d(dst + kHalfBytes, &tm_x, c0 + 64, r0, bars.full(s));
+    }
   };
   auto drain_loads = [&]() {
     for (int64_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
@@ -423,15 +432,25 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
         __syncwarp();
       }
       if (lane == 0) {
+        const uint64_t pol = (MXQ_DUAL_L2_HINTS & 2) ? l2_policy_evict_first() : 0ull;
         if (R::kRow) {
-          tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
-                       base + kOffQRow + b * kQTileBytes);
+          if (MXQ_DUAL_L2_HINTS & 2)
+            tma_store_2d_hint(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
+                              base + kOffQRow + b * kQTileBytes, pol);
+          else
+            tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
+                         base + kOffQRow + b * kQTileBytes);
           bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
                      kAtomBytes);
         }
-        if (R::kCol)
-          tma_store_2d(&tm_qcol, static_cast<int32_t>(row0), static_cast<int32_t>(tj * kTile),
-                       base + kOffQCol + b * kQTileBytes);
+        if (R::kCol) {
+          if (MXQ_DUAL_L2_HINTS & 2)
+            tma_store_2d_hint(&tm_qcol, static_cast<int32_t>(row0), static_cast<int32_t>(tj * kTile),
+                              base + kOffQCol + b * kQTileBytes, pol);
+          else
+            tma_store_2d(&tm_qcol, static_cast<int32_t>(row0), static_cast<int32_t>(tj * kTile),
+                         base + kOffQCol + b * kQTileBytes);
+        }
         if (kMode == kDual) {
           if (row0 < end_rows) {
             int64_t lo = 0, hi = Mrows;
@@ -601,6 +620,37 @@ extern "C" int mxq_quantize_32x1(const void* x, int64_t M, int64_t N, uint8_t* q
                           {reinterpret_cast<uintptr_t>(s_rm), MN / 32}};
   if (ranges_overlap(r, 3)) return MXQ_EOVERLAP;
   return launch_tiles<kColOnly>(x, M, N, nullptr, 0, nullptr, nullptr, q_col, s_rm, stream);
+}
+
+namespace {
+// Diagnostic kernel: one warp waits, with the pipelines' bounded wait, on an
+// mbarrier that nothing ever arrives on, so the wait runs out after limit_ns
+// and records MXQ_DEV_TIMEOUT exactly as a stalled pipeline would.
+__global__ void mxq_selftest_timeout_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_bounded(smem_u32(&bar), 0u, &abort_flag, &g_mxq_status,
+                                    MXQ_DEV_TIMEOUT, limit_ns);
+  (void)__all_sync(0xFFFFFFFFu, ok);
+}
+
+}  // namespace
+
+extern "C" int mxq_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1000000ull || limit_ns > 4000000000ull) return MXQ_EBADSHAPE;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, mxq_selftest_timeout_kernel, limit_ns) == cudaSuccess
+             ? MXQ_OK
+             : MXQ_ECUDA;
 }
 
 namespace mxq {
