@@ -29,6 +29,9 @@ import numpy as np
 _HERE = pathlib.Path(__file__).resolve().parent
 _SRC = _HERE / "mxq_oracle.c"
 _LIB = _HERE / "libmxq_oracle.so"
+# A prebuilt oracle library to load instead (the mutation test points this at
+# deliberately broken copies to show that the pins catch them).
+_LIB_OVERRIDE = os.environ.get("MXQ_ORACLE_LIB")
 
 F32 = 0
 BF16 = 1
@@ -58,7 +61,7 @@ _lib_handle = None
 def _lib():
     global _lib_handle
     if _lib_handle is None:
-        lib = ctypes.CDLL(str(build()))
+        lib = ctypes.CDLL(_LIB_OVERRIDE if _LIB_OVERRIDE else str(build()))
         p = ctypes.c_void_p
         i64 = ctypes.c_int64
         lib.oracle_e4m3_value.restype = ctypes.c_double
