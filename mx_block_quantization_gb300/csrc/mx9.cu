@@ -9,9 +9,13 @@
 //
 // pack: persistent and warp-specialized like the dual-axis kernel.  One
 // producer warp streams contiguous runs of blocks into a shared-memory
-// ring with 1-D bulk copies (TMA); each consumer thread then owns one whole
-// 16-element block, so exponents and prime bits need no shuffles, and writes
-// its 16 q bytes, exponent byte and prime byte with coalesced stores.
+// ring with 1-D bulk copies (TMA); each consumer thread then owns whole
+// 16-element blocks (one per stage for fp32, two for bf16), so exponents and
+// prime bits need no shuffles, and writes their 16 q bytes, exponent byte and
+// prime byte with coalesced stores.  Finite blocks round with one FMA against
+// 1.5 * 2^23 and clamp two elements at once as int16 pairs; bf16 blocks take
+// their exponent maximum on the packed words and feed the bf16 halves to a
+// mixed-precision FMA, which keeps the integer pipe (the limit for bf16) light.
 // unpack: a streaming kernel, one wave of resident blocks, 4 lanes per block,
 // exact q * 2^k built without conversion instructions.
 #include <cuda_runtime.h>
@@ -34,13 +38,25 @@ using namespace mxq;
 #define MXQ_MX9_PACK_F32_RING_KB 64
 #endif
 #ifndef MXQ_MX9_PACK_BF16_WARPS
-#define MXQ_MX9_PACK_BF16_WARPS 12
+#define MXQ_MX9_PACK_BF16_WARPS 8
 #endif
 #ifndef MXQ_MX9_PACK_BF16_RING_KB
-#define MXQ_MX9_PACK_BF16_RING_KB 96
+#define MXQ_MX9_PACK_BF16_RING_KB 48
 #endif
 #ifndef MXQ_MX9_PACK_CTAS_PER_SM
 #define MXQ_MX9_PACK_CTAS_PER_SM 2
+#endif
+#ifndef MXQ_MX9_PACK_FMA_ROUND
+#define MXQ_MX9_PACK_FMA_ROUND 1
+#endif
+#ifndef MXQ_MX9_PACK_BF16_PER_THREAD
+#define MXQ_MX9_PACK_BF16_PER_THREAD 2
+#endif
+#ifndef MXQ_MX9_PACK_F32_PER_THREAD
+#define MXQ_MX9_PACK_F32_PER_THREAD 1
+#endif
+#ifndef MXQ_MX9_PACK_MIXED_FMA
+#define MXQ_MX9_PACK_MIXED_FMA 1
 #endif
 #ifndef MXQ_MX9_UNPACK_UNROLL
 #define MXQ_MX9_UNPACK_UNROLL 4
@@ -52,13 +68,16 @@ constexpr int kUnrollUnpack = MXQ_MX9_UNPACK_UNROLL;
 // Sticky status word of this file's kernels (MXQ_DEV_* bits).
 __device__ unsigned int g_mx9_status = 0;
 
-// Pack kernel shape per input type: consumer warps (one 16-element block per
-// consumer thread and stage), one producer warp, a ring of stages.
+// Pack kernel shape per input type: consumer warps (kPerThread 16-element
+// blocks per consumer thread and stage), one producer warp, a ring of stages.
+// Rings deeper than these measured slower.
 template <bool kBF16>
 struct PackShape {
   static constexpr int kWarps = kBF16 ? MXQ_MX9_PACK_BF16_WARPS : MXQ_MX9_PACK_F32_WARPS;
+  static constexpr int kPerThread = kBF16 ? MXQ_MX9_PACK_BF16_PER_THREAD : MXQ_MX9_PACK_F32_PER_THREAD;
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kBlocksPerStage = kWarps * 32;
+  static constexpr int kConsumers = kWarps * 32;
+  static constexpr int kBlocksPerStage = kConsumers * kPerThread;
   static constexpr uint32_t kBlockBytes = kBF16 ? 32u : 64u;  // 16 elements
   static constexpr uint32_t kStageBytes = kBlocksPerStage * kBlockBytes;
   static constexpr uint32_t kRingBytes =
@@ -93,6 +112,44 @@ __device__ __forceinline__ uint32_t q_byte(float x, float mult) {
   return static_cast<uint32_t>(max(-127, min(127, r))) & 0xFFu;
 }
 
+__device__ __forceinline__ float fma_rn_noftz(float a, float b, float c) {
+  float r;
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Two elements of a finite block: round_half_even(x * mult) clamped to
+// [-127, 127], as two int16 in one word.  For |x * mult| < 2^22 the FMA
+// 1.5 * 2^23 + x * mult rounds once, half to even, to an integer whose
+// two's-complement value sits in the low 16 bits of the result; a finite
+// block gives |x * mult| < 2^8.
+__device__ __forceinline__ uint32_t q_pair_s16x2(uint32_t a, uint32_t b, float mult) {
+  const float ra = fma_rn_noftz(__uint_as_float(a), mult, 12582912.0f);
+  const float rb = fma_rn_noftz(__uint_as_float(b), mult, 12582912.0f);
+  uint32_t h = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x5410);
+  asm("max.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0xFF81FF81u));
+  asm("min.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0x007F007Fu));
+  return h;
+}
+
+// q_pair_s16x2 on the two bf16 halves of w without widening them: the
+// mixed-precision FMA takes bf16 factors and an fp32 addend and rounds once.
+// mult_bits: the fp32 power-of-two multiplier, exact as bf16 (its high half).
+__device__ __forceinline__ uint32_t q_pair_s16x2_bf16(uint32_t w, uint32_t mult_bits) {
+  float ra, rb;
+  asm("{\n\t.reg .b16 xl, xh, ml, mh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "mov.b32 {ml, mh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, xl, mh, %4;\n\t"
+      "fma.rn.f32.bf16 %1, xh, mh, %4;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "r"(w), "r"(mult_bits), "f"(12582912.0f));
+  uint32_t h = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x5410);
+  asm("max.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0xFF81FF81u));
+  asm("min.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0x007F007Fu));
+  return h;
+}
+
 // One block of 16 elements given as 16 fp32 bit patterns.
 __device__ __forceinline__ void pack_block(const uint32_t* f, uint4* q, uint32_t* eb_out,
                                            uint32_t* prime_out) {
@@ -104,6 +161,22 @@ __device__ __forceinline__ void pack_block(const uint32_t* f, uint4* q, uint32_t
     eb = max(eb, pe[p]);
   }
   const uint32_t eb8 = eb >> 23;
+  if (MXQ_MX9_PACK_FMA_ROUND && eb8 != 255u) {
+    // finite block (no Inf or NaN): rounding by FMA, clamping on int16 pairs
+    const float m0 = pair_multiplier(eb8, 0u), m1 = pair_multiplier(eb8, 1u);
+    uint32_t bits = 0, h[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const uint32_t t = pe[p] < eb;
+      bits |= t << p;
+      h[p] = q_pair_s16x2(f[2 * p], f[2 * p + 1], t ? m1 : m0);
+    }
+    *q = make_uint4(__byte_perm(h[0], h[1], 0x6420), __byte_perm(h[2], h[3], 0x6420),
+                    __byte_perm(h[4], h[5], 0x6420), __byte_perm(h[6], h[7], 0x6420));
+    *eb_out = eb8;
+    *prime_out = bits;
+    return;
+  }
   uint32_t bits = 0, word[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
@@ -115,6 +188,55 @@ __device__ __forceinline__ void pack_block(const uint32_t* f, uint4* q, uint32_t
     word[p >> 1] |= two << (16 * (p & 1));
   }
   *q = make_uint4(word[0], word[1], word[2], word[3]);
+  *eb_out = eb8;
+  *prime_out = bits;
+}
+
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// One block of 16 bf16 elements given as 8 words, word p = pair p (element 2p
+// in the low half).  Exponent fields are compared in place, two per word; a
+// pair is demoted when both of its fields are below the block's: with
+// e16 = block field << 7, the low half of (w & 0x7F80) + 0x8000 - e16 reaches
+// bit 15 exactly when the element's field is >= the block's, and likewise for
+// the high half at bit 31 (the low half cannot carry).
+__device__ __forceinline__ void pack_block_bf16(const uint32_t* w, uint4* q, uint32_t* eb_out,
+                                                uint32_t* prime_out) {
+  uint32_t m[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) m[p] = w[p] & 0x7F807F80u;
+  const uint32_t mx = vmax_u16x2(vmax_u16x2(vmax_u16x2(m[0], m[1]), vmax_u16x2(m[2], m[3])),
+                                 vmax_u16x2(vmax_u16x2(m[4], m[5]), vmax_u16x2(m[6], m[7])));
+  const uint32_t e16 = max(mx & 0xFFFFu, mx >> 16);
+  const uint32_t eb8 = e16 >> 7;
+  if (!MXQ_MX9_PACK_FMA_ROUND || eb8 == 255u) {
+    uint32_t f[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      f[2 * k] = w[k] << 16;                 // exact widening of each bf16
+      f[2 * k + 1] = w[k] & 0xFFFF0000u;
+    }
+    pack_block(f, q, eb_out, prime_out);
+    return;
+  }
+  const uint32_t d2 = (0x8000u - e16) * 0x10001u;
+  const float m0 = pair_multiplier(eb8, 0u), m1 = pair_multiplier(eb8, 1u);
+  uint32_t bits = 0, h[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t t = ((m[p] + d2) & 0x80008000u) == 0u;
+    bits |= t << p;
+    if (MXQ_MX9_PACK_MIXED_FMA)
+      h[p] = q_pair_s16x2_bf16(w[p], __float_as_uint(t ? m1 : m0));
+    else
+      h[p] = q_pair_s16x2(w[p] << 16, w[p] & 0xFFFF0000u, t ? m1 : m0);
+  }
+  *q = make_uint4(__byte_perm(h[0], h[1], 0x6420), __byte_perm(h[2], h[3], 0x6420),
+                  __byte_perm(h[4], h[5], 0x6420), __byte_perm(h[6], h[7], 0x6420));
   *eb_out = eb8;
   *prime_out = bits;
 }
@@ -178,19 +300,21 @@ __global__ void __launch_bounds__(PackShape<kBF16>::kThreads, MXQ_MX9_PACK_CTAS_
     const bool ok = mbar_wait_bounded(full(s), static_cast<uint32_t>((i / S::kStages) & 1),
                                       abort_flag, &g_mx9_status, MXQ_DEV_TIMEOUT);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
-    const int64_t blk = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * S::kBlocksPerStage + tid;
-    if (blk < nb) {
-      const uint32_t src = base + static_cast<uint32_t>(s) * S::kStageBytes + tid * S::kBlockBytes;
-      uint32_t f[16];
+    const int64_t blk0 = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * S::kBlocksPerStage;
+#pragma unroll
+    for (int j = 0; j < S::kPerThread; ++j) {
+      const int local = j * S::kConsumers + tid;
+      const int64_t blk = blk0 + local;
+      if (blk >= nb) break;
+      const uint32_t src = base + static_cast<uint32_t>(s) * S::kStageBytes + local * S::kBlockBytes;
+      uint4 qv;
+      uint32_t eb8, bits;
       if (kBF16) {
         const uint4 a = lds128(src), b = lds128(src + 16);
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          f[2 * k] = w[k] << 16;             // exact widening of each bf16
-          f[2 * k + 1] = w[k] & 0xFFFF0000u;
-        }
+        pack_block_bf16(w, &qv, &eb8, &bits);
       } else {
+        uint32_t f[16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint4 a = lds128(src + 16u * k);
@@ -199,10 +323,8 @@ __global__ void __launch_bounds__(PackShape<kBF16>::kThreads, MXQ_MX9_PACK_CTAS_
           f[4 * k + 2] = a.z;
           f[4 * k + 3] = a.w;
         }
+        pack_block(f, &qv, &eb8, &bits);
       }
-      uint4 qv;
-      uint32_t eb8, bits;
-      pack_block(f, &qv, &eb8, &bits);
       __stcs(q + blk, qv);
       max_exp[blk] = static_cast<uint8_t>(eb8);
       prime[blk] = static_cast<uint8_t>(bits);
