@@ -16,8 +16,9 @@
 // 1.5 * 2^23 and clamp two elements at once as int16 pairs; bf16 blocks take
 // their exponent maximum on the packed words and feed the bf16 halves to a
 // mixed-precision FMA, which keeps the integer pipe (the limit for bf16) light.
-// unpack: a streaming kernel, one wave of resident blocks, 4 lanes per block,
-// exact q * 2^k built without conversion instructions.
+// unpack: a streaming kernel, one wave of resident blocks; each lane writes 16
+// output bytes (4 fp32 or 8 bf16 elements), exact q * 2^k built without
+// conversion instructions.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -58,12 +59,14 @@ using namespace mxq;
 #ifndef MXQ_MX9_PACK_MIXED_FMA
 #define MXQ_MX9_PACK_MIXED_FMA 1
 #endif
-#ifndef MXQ_MX9_UNPACK_UNROLL
-#define MXQ_MX9_UNPACK_UNROLL 4
+#ifndef MXQ_MX9_UNPACK_UNROLL_F32
+#define MXQ_MX9_UNPACK_UNROLL_F32 2
+#endif
+#ifndef MXQ_MX9_UNPACK_UNROLL_BF16
+#define MXQ_MX9_UNPACK_UNROLL_BF16 4
 #endif
 
 constexpr int kUnpackBlock = 256;
-constexpr int kUnrollUnpack = MXQ_MX9_UNPACK_UNROLL;
 
 // Sticky status word of this file's kernels (MXQ_DEV_* bits).
 __device__ unsigned int g_mx9_status = 0;
@@ -355,48 +358,75 @@ __device__ __forceinline__ float small_int_to_float(int32_t q) {
   return fadd_rn_noftz(__int_as_float(0x4B400000 + q), -12582912.0f);
 }
 
-// 4 lanes per block, 4 elements per lane; q * 2^k is exact (|q| <= 127,
-// k >= -126) except for overflow in max_exp 255 blocks.
+// A lane writes 16 output bytes: 4 fp32 or 8 bf16 elements, so 4 (fp32) or
+// 2 (bf16) lanes share a block.  q * 2^k is exact (|q| <= 127, k >= -126)
+// except for overflow in max_exp 255 blocks; a bf16 result has at most 7
+// significant bits, so the top half of the fp32 is the exact bf16.
+template <bool kBF16>
+struct UnpackLane {
+  static constexpr int kElems = kBF16 ? 8 : 4;
+  static constexpr int kLanesPerBlock = 16 / kElems;
+  static constexpr int kUnroll = kBF16 ? MXQ_MX9_UNPACK_UNROLL_BF16 : MXQ_MX9_UNPACK_UNROLL_F32;
+};
+
+__device__ __forceinline__ void unpack4(uint32_t w, float s0, float s1, float* y) {
+  const int32_t v = static_cast<int32_t>(w);
+  y[0] = fmul_rn_noftz(small_int_to_float((v << 24) >> 24), s0);
+  y[1] = fmul_rn_noftz(small_int_to_float((v << 16) >> 24), s0);
+  y[2] = fmul_rn_noftz(small_int_to_float((v << 8) >> 24), s1);
+  y[3] = fmul_rn_noftz(small_int_to_float(v >> 24), s1);
+}
+
 template <bool kBF16>
 __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
     const uint32_t* __restrict__ q, const uint8_t* __restrict__ max_exp,
     const uint8_t* __restrict__ prime, void* __restrict__ y, int64_t nchunks) {
+  using U = UnpackLane<kBF16>;
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kUnpackBlock;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kUnpackBlock + (threadIdx.x - lane);
-  for (int64_t base = warp0; base < nchunks; base += stride * kUnrollUnpack) {
-    uint32_t qv[kUnrollUnpack], ev[kUnrollUnpack], pv[kUnrollUnpack];
+  // pairs handled by this lane inside its block, and their prime-bit shift
+  const int pshift = (lane % U::kLanesPerBlock) * (U::kElems / 2);
+  for (int64_t base = warp0; base < nchunks; base += stride * U::kUnroll) {
+    uint32_t qv[U::kUnroll][U::kElems / 4], ev[U::kUnroll], pv[U::kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnrollUnpack; ++u) {
+    for (int u = 0; u < U::kUnroll; ++u) {
       const int64_t c = base + u * stride + lane;
       if (c < nchunks) {
-        qv[u] = __ldcs(q + c);
-        ev[u] = __ldg(max_exp + (c >> 2));
-        pv[u] = __ldg(prime + (c >> 2));
+        if (kBF16) {
+          const uint2 w = __ldcs(reinterpret_cast<const uint2*>(q) + c);
+          qv[u][0] = w.x;
+          qv[u][U::kElems / 4 - 1] = w.y;
+        } else {
+          qv[u][0] = __ldcs(q + c);
+        }
+        ev[u] = __ldg(max_exp + c / U::kLanesPerBlock);
+        pv[u] = __ldg(prime + c / U::kLanesPerBlock);
       } else {
-        qv[u] = ev[u] = pv[u] = 0;
+        qv[u][0] = qv[u][U::kElems / 4 - 1] = ev[u] = pv[u] = 0;
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnrollUnpack; ++u) {
+    for (int u = 0; u < U::kUnroll; ++u) {
       const int64_t c = base + u * stride + lane;
       if (c >= nchunks) continue;
       const int E = static_cast<int>(ev[u]) - 127;
-      const int pbits = static_cast<int>(pv[u] >> (2 * (lane & 3)));
-      const float s0 = exp2_normal(max(E - 6 - (pbits & 1), -126));
-      const float s1 = exp2_normal(max(E - 6 - ((pbits >> 1) & 1), -126));
-      const int32_t w = static_cast<int32_t>(qv[u]);
-      const float y0 = fmul_rn_noftz(small_int_to_float((w << 24) >> 24), s0);
-      const float y1 = fmul_rn_noftz(small_int_to_float((w << 16) >> 24), s0);
-      const float y2 = fmul_rn_noftz(small_int_to_float((w << 8) >> 24), s1);
-      const float y3 = fmul_rn_noftz(small_int_to_float(w >> 24), s1);
+      const int pbits = static_cast<int>(pv[u] >> pshift);
+      float s[U::kElems / 2];
+#pragma unroll
+      for (int k = 0; k < U::kElems / 2; ++k)
+        s[k] = exp2_normal(max(E - 6 - ((pbits >> k) & 1), -126));
+      float v[U::kElems];
+#pragma unroll
+      for (int k = 0; k < U::kElems / 4; ++k) unpack4(qv[u][k], s[2 * k], s[2 * k + 1], v + 4 * k);
       if (kBF16) {
-        // at most 7 significant bits: the top half of the fp32 is the exact bf16
-        const uint32_t lo = (__float_as_uint(y0) >> 16) | (__float_as_uint(y1) & 0xFFFF0000u);
-        const uint32_t hi = (__float_as_uint(y2) >> 16) | (__float_as_uint(y3) & 0xFFFF0000u);
-        __stcs(reinterpret_cast<uint2*>(y) + c, make_uint2(lo, hi));
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          o[k] = (__float_as_uint(v[2 * k]) >> 16) | (__float_as_uint(v[2 * k + 1]) & 0xFFFF0000u);
+        __stcs(reinterpret_cast<uint4*>(y) + c, make_uint4(o[0], o[1], o[2], o[3]));
       } else {
-        __stcs(reinterpret_cast<float4*>(y) + c, make_float4(y0, y1, y2, y3));
+        __stcs(reinterpret_cast<float4*>(y) + c, make_float4(v[0], v[1], v[2], v[3]));
       }
     }
   }
@@ -504,7 +534,7 @@ extern "C" int mx9_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
   const int sms = sm_count_current_device(nullptr);
   if (sms <= 0) return MXQ_ECUDA;
 
-  const int64_t nchunks = n / 4;
+  const int64_t nchunks = n / (dtype == MXQ_F32 ? UnpackLane<false>::kElems : UnpackLane<true>::kElems);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dtype == MXQ_F32 ? unpack_grid(mx9_unpack_kernel<false>, nchunks, sms)
                                       : unpack_grid(mx9_unpack_kernel<true>, nchunks, sms));

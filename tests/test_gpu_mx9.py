@@ -141,3 +141,27 @@ def test_rejections_through_binding():
     assert e.value.code == mxq.EBADSHAPE
     with pytest.raises(ValueError):
         mxq.mx9_pack(torch.zeros((4, 16), dtype=torch.float16, device="cuda"))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(256, 1024), (300, 1040)])
+def test_unpack_with_unaligned_exponent_and_prime_pointers(rows, cols, dt):
+    """max_exp and prime may start at any byte (the ABI asks alignment of q and
+    the output only): byte-offset views give the oracle's bytes."""
+    x = W.mx9_outliers(rows, cols, seed=11)
+    if dt == "bf16":
+        x = W.f32_to_bf16_bits(x)
+    nb = rows * cols // 16
+    q, e, p = mxq.mx9_pack(_dev(x))
+    e_big = torch.zeros(nb + 3, dtype=torch.uint8, device="cuda")
+    p_big = torch.zeros(nb + 5, dtype=torch.uint8, device="cuda")
+    e_big[3:].copy_(e)
+    p_big[5:].copy_(p.reshape(-1))
+    rq, re, rp = oracle.mx9_pack(x)
+    for out_dtype, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+        y = _fill_like((rows, cols), out_dtype)
+        mxq.mx9_unpack(q, e_big[3:], p_big[5:], out_dtype, (rows, cols), out=y)
+        ry = oracle.mx9_unpack(rq, re, rp, name, rows, cols)
+        torch.cuda.synchronize()
+        got = y.cpu().view(torch.int32 if name == "f32" else torch.int16).numpy()
+        assert_bytes_equal(got.view(np.uint8), ry.view(np.uint8), f"unaligned unpack {name}")
