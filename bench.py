@@ -598,6 +598,17 @@ def run_case(args):
             torch.bfloat16).to(dev)
         for _ in range(args.warmup):
             mxq.quantize_2d_dual(x, offs)
+    elif args.case.startswith("rec_"):
+        # the single packed tensor of MX9 (--fmt 9) or MX6 (--fmt 6) records, rows blocked
+        tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
+        xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
+        rec = mxq.mx_pack_packed(xm, args.fmt, 1)
+        y = torch.empty_like(xm)
+        for _ in range(args.warmup):
+            if args.case.startswith("rec_pack"):
+                mxq.mx_pack_packed(xm, args.fmt, 1, out=rec)
+            else:
+                mxq.mx_unpack_packed(rec, args.fmt, y, 1)
     else:
         tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
         xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
@@ -609,7 +620,8 @@ def run_case(args):
                 mxq.mx9_unpack(q, e, p, tdt, (M, N))
     torch.cuda.synchronize()
     assert mxq.device_status(clear=True) == 0
-    print(json.dumps({"case": args.case, "shape": [M, N], "launches": args.warmup}))
+    print(json.dumps({"case": args.case, "shape": [M, N], "launches": args.warmup,
+                      **({"fmt": args.fmt} if args.case.startswith("rec_") else {})}))
     return 0
 
 
@@ -624,9 +636,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="also print one line per throughput-sweep shape (graph replay)")
-    ap.add_argument("--case", choices=["dual", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16"],
+    ap.add_argument("--case", choices=["dual", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16",
+                                       "rec_pack_f32", "rec_pack_bf16", "rec_unpack_f32",
+                                       "rec_unpack_bf16"],
                     help="only launch this kernel --warmup times on --shape (profiling)")
     ap.add_argument("--shape", default="16384x7168")
+    ap.add_argument("--fmt", type=int, choices=[9, 6], default=9,
+                    help="with --case rec_*: MX9 or MX6 records")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --case dual: that many K-groups and a 1/8 uncovered tail")
     args = ap.parse_args(argv)

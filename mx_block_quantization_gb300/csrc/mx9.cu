@@ -23,6 +23,7 @@
 #include <stdint.h>
 
 #include "mxq.h"
+#include "mx_block.cuh"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
 
@@ -47,17 +48,11 @@ using namespace mxq;
 #ifndef MXQ_MX9_PACK_CTAS_PER_SM
 #define MXQ_MX9_PACK_CTAS_PER_SM 2
 #endif
-#ifndef MXQ_MX9_PACK_FMA_ROUND
-#define MXQ_MX9_PACK_FMA_ROUND 1
-#endif
 #ifndef MXQ_MX9_PACK_BF16_PER_THREAD
 #define MXQ_MX9_PACK_BF16_PER_THREAD 2
 #endif
 #ifndef MXQ_MX9_PACK_F32_PER_THREAD
 #define MXQ_MX9_PACK_F32_PER_THREAD 1
-#endif
-#ifndef MXQ_MX9_PACK_MIXED_FMA
-#define MXQ_MX9_PACK_MIXED_FMA 1
 #endif
 #ifndef MXQ_MX9_UNPACK_PRMT_F32
 #define MXQ_MX9_UNPACK_PRMT_F32 0
@@ -77,10 +72,15 @@ constexpr int kUnpackBlock = 256;
 // Sticky status word of this file's kernels (MXQ_DEV_* bits).
 __device__ unsigned int g_mx9_status = 0;
 
+// Output forms of the pack kernel: the split tensors (q, max_exp, prime), or
+// one packed tensor of block records (MX9: 18 bytes, MX6: 12 bytes).
+enum PackOut { kSplit = 0, kRecMx9 = MXQ_FMT_MX9, kRecMx6 = MXQ_FMT_MX6 };
+
 // Pack kernel shape per input type: consumer warps (kPerThread 16-element
-// blocks per consumer thread and stage), one producer warp, a ring of stages.
-// Rings deeper than these measured slower.
-template <bool kBF16>
+// blocks per consumer thread and stage), one producer warp, a ring of stages,
+// and for record outputs a per-warp staging area of 32 records.  Rings deeper
+// than these measured slower.
+template <bool kBF16, int kOut>
 struct PackShape {
   static constexpr int kWarps = kBF16 ? MXQ_MX9_PACK_BF16_WARPS : MXQ_MX9_PACK_F32_WARPS;
   static constexpr int kPerThread = kBF16 ? MXQ_MX9_PACK_BF16_PER_THREAD : MXQ_MX9_PACK_F32_PER_THREAD;
@@ -92,11 +92,16 @@ struct PackShape {
   static constexpr uint32_t kRingBytes =
       (kBF16 ? MXQ_MX9_PACK_BF16_RING_KB : MXQ_MX9_PACK_F32_RING_KB) * 1024u;
   static constexpr int kStages = static_cast<int>(kRingBytes / kStageBytes);
+  static constexpr uint32_t kRecord =
+      kOut == kRecMx9 ? MXQ_MX9_RECORD_BYTES : kOut == kRecMx6 ? MXQ_MX6_RECORD_BYTES : 0u;
   static constexpr uint32_t kOffBar = kStages * kStageBytes;
   static constexpr uint32_t kOffFlag = kOffBar + 16u * kStages;
-  static constexpr uint32_t kSmemBytes = kOffFlag + 16u + 128u;  // + alignment slack
+  static constexpr uint32_t kOffRec = kOffFlag + 16u;
+  static constexpr uint32_t kRunBytes = 32u * kRecord;  // one warp's 32 records
+  static constexpr uint32_t kSmemBytes = kOffRec + kWarps * 2u * kRunBytes + 128u;  // + alignment
   static_assert(kStages >= 2, "ring too small");
-  static_assert(kSmemBytes <= 227u * 1024u, "shared memory budget");
+  static_assert((32u * kRecord) % 16u == 0, "record runs of a warp stay 16-byte aligned");
+  static_assert(kSmemBytes * MXQ_MX9_PACK_CTAS_PER_SM <= 227u * 1024u, "shared memory budget");
 };
 
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
@@ -108,153 +113,55 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
       : "memory");
 }
 
-// Multiplier 2^-k of a pair from the block's exponent field eb8 (E = eb8 - 127)
-// and the pair's prime bit t: k = max(E - 6 - t, -126), 127 - k = min(260 - eb8 + t, 253).
-__device__ __forceinline__ float pair_multiplier(uint32_t eb8, uint32_t t) {
-  return __uint_as_float(min(260u - eb8 + t, 253u) << 23);
-}
-
-// x * 2^-k (exact multiply, no flush) rounded half-to-even to an integer and
-// clamped to [-127, 127]; cvt.rni gives 0 for NaN and saturates +-Inf.
-__device__ __forceinline__ uint32_t q_byte(float x, float mult) {
-  const int r = __float2int_rn(fmul_rn_noftz(x, mult));
-  return static_cast<uint32_t>(max(-127, min(127, r))) & 0xFFu;
-}
-
-__device__ __forceinline__ float fma_rn_noftz(float a, float b, float c) {
-  float r;
-  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Two elements of a finite block: round_half_even(x * mult) clamped to
-// [-127, 127], as two int16 in one word.  For |x * mult| < 2^22 the FMA
-// 1.5 * 2^23 + x * mult rounds once, half to even, to an integer whose
-// two's-complement value sits in the low 16 bits of the result; a finite
-// block gives |x * mult| < 2^8.
-__device__ __forceinline__ uint32_t q_pair_s16x2(uint32_t a, uint32_t b, float mult) {
-  const float ra = fma_rn_noftz(__uint_as_float(a), mult, 12582912.0f);
-  const float rb = fma_rn_noftz(__uint_as_float(b), mult, 12582912.0f);
-  uint32_t h = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x5410);
-  asm("max.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0xFF81FF81u));
-  asm("min.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0x007F007Fu));
-  return h;
-}
-
-// q_pair_s16x2 on the two bf16 halves of w without widening them: the
-// mixed-precision FMA takes bf16 factors and an fp32 addend and rounds once.
-// mult_bits: the fp32 power-of-two multiplier, exact as bf16 (its high half).
-__device__ __forceinline__ uint32_t q_pair_s16x2_bf16(uint32_t w, uint32_t mult_bits) {
-  float ra, rb;
-  asm("{\n\t.reg .b16 xl, xh, ml, mh;\n\t"
-      "mov.b32 {xl, xh}, %2;\n\t"
-      "mov.b32 {ml, mh}, %3;\n\t"
-      "fma.rn.f32.bf16 %0, xl, mh, %4;\n\t"
-      "fma.rn.f32.bf16 %1, xh, mh, %4;\n\t}"
-      : "=f"(ra), "=f"(rb)
-      : "r"(w), "r"(mult_bits), "f"(12582912.0f));
-  uint32_t h = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x5410);
-  asm("max.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0xFF81FF81u));
-  asm("min.s16x2 %0, %0, %1;" : "+r"(h) : "r"(0x007F007Fu));
-  return h;
-}
-
-// One block of 16 elements given as 16 fp32 bit patterns.
-__device__ __forceinline__ void pack_block(const uint32_t* f, uint4* q, uint32_t* eb_out,
-                                           uint32_t* prime_out) {
-  uint32_t pe[8];
-  uint32_t eb = 0;
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    pe[p] = max(f[2 * p] & 0x7F800000u, f[2 * p + 1] & 0x7F800000u);
-    eb = max(eb, pe[p]);
+// Copy a warp's staged records (16-byte aligned on both sides, an even
+// number of bytes) to global memory: 16-byte units, then 2-byte pieces.
+__device__ __forceinline__ void copy_records_out(uint8_t* g, uint32_t s, uint32_t bytes, int lane) {
+  const uint32_t n16 = bytes >> 4;
+  for (uint32_t i = lane; i < n16; i += 32) __stcs(reinterpret_cast<uint4*>(g) + i, lds128(s + 16u * i));
+  const uint32_t h0 = n16 * 8u, nh = bytes >> 1;
+  for (uint32_t i = h0 + lane; i < nh; i += 32) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(s + 2u * i));
+    reinterpret_cast<uint16_t*>(g)[i] = static_cast<uint16_t>(v);
   }
-  const uint32_t eb8 = eb >> 23;
-  if (MXQ_MX9_PACK_FMA_ROUND && eb8 != 255u) {
-    // finite block (no Inf or NaN): rounding by FMA, clamping on int16 pairs
-    const float m0 = pair_multiplier(eb8, 0u), m1 = pair_multiplier(eb8, 1u);
-    uint32_t bits = 0, h[8];
+}
+
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Stage one block record at shared address a: [exponent, prime, data].
+template <int kOut>
+__device__ __forceinline__ void stage_record(uint32_t a, uint32_t eb8, uint32_t bits,
+                                             const uint32_t* h) {
+  const uint32_t head = eb8 | (bits << 8);
+  if (kOut == kRecMx9) {  // 18 bytes at a 2-byte aligned address
+    const uint4 q = pairs_to_bytes(h);
+    const uint32_t w[5] = {head | (q.x << 16), __byte_perm(q.x, q.y, 0x5432),
+                           __byte_perm(q.y, q.z, 0x5432), __byte_perm(q.z, q.w, 0x5432), q.w >> 16};
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const uint32_t t = pe[p] < eb;
-      bits |= t << p;
-      h[p] = q_pair_s16x2(f[2 * p], f[2 * p + 1], t ? m1 : m0);
+    for (int k = 0; k < 4; ++k) {
+      sts16(a + 4u * k, w[k] & 0xFFFFu);
+      sts16(a + 4u * k + 2u, w[k] >> 16);
     }
-    *q = make_uint4(__byte_perm(h[0], h[1], 0x6420), __byte_perm(h[2], h[3], 0x6420),
-                    __byte_perm(h[4], h[5], 0x6420), __byte_perm(h[6], h[7], 0x6420));
-    *eb_out = eb8;
-    *prime_out = bits;
-    return;
+    sts16(a + 16u, w[4]);
+  } else {  // MX6: 12 bytes at a 4-byte aligned address
+    uint32_t lo, mid, hi;
+    pairs_to_codes5(h, &lo, &mid, &hi);
+    sts32(a, head | (lo << 16));
+    sts32(a + 4u, (lo >> 16) | (mid << 16));
+    sts32(a + 8u, (mid >> 16) | (hi << 16));
   }
-  uint32_t bits = 0, word[4] = {0, 0, 0, 0};
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const uint32_t t = pe[p] < eb;
-    bits |= t << p;
-    const float m = pair_multiplier(eb8, t);
-    const uint32_t two = q_byte(__uint_as_float(f[2 * p]), m) |
-                         (q_byte(__uint_as_float(f[2 * p + 1]), m) << 8);
-    word[p >> 1] |= two << (16 * (p & 1));
-  }
-  *q = make_uint4(word[0], word[1], word[2], word[3]);
-  *eb_out = eb8;
-  *prime_out = bits;
 }
 
-__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// One block of 16 bf16 elements given as 8 words, word p = pair p (element 2p
-// in the low half).  Exponent fields are compared in place, two per word; a
-// pair is demoted when both of its fields are below the block's: with
-// e16 = block field << 7, the low half of (w & 0x7F80) + 0x8000 - e16 reaches
-// bit 15 exactly when the element's field is >= the block's, and likewise for
-// the high half at bit 31 (the low half cannot carry).
-__device__ __forceinline__ void pack_block_bf16(const uint32_t* w, uint4* q, uint32_t* eb_out,
-                                                uint32_t* prime_out) {
-  uint32_t m[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) m[p] = w[p] & 0x7F807F80u;
-  const uint32_t mx = vmax_u16x2(vmax_u16x2(vmax_u16x2(m[0], m[1]), vmax_u16x2(m[2], m[3])),
-                                 vmax_u16x2(vmax_u16x2(m[4], m[5]), vmax_u16x2(m[6], m[7])));
-  const uint32_t e16 = max(mx & 0xFFFFu, mx >> 16);
-  const uint32_t eb8 = e16 >> 7;
-  if (!MXQ_MX9_PACK_FMA_ROUND || eb8 == 255u) {
-    uint32_t f[16];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      f[2 * k] = w[k] << 16;                 // exact widening of each bf16
-      f[2 * k + 1] = w[k] & 0xFFFF0000u;
-    }
-    pack_block(f, q, eb_out, prime_out);
-    return;
-  }
-  const uint32_t d2 = (0x8000u - e16) * 0x10001u;
-  const float m0 = pair_multiplier(eb8, 0u), m1 = pair_multiplier(eb8, 1u);
-  uint32_t bits = 0, h[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const uint32_t t = ((m[p] + d2) & 0x80008000u) == 0u;
-    bits |= t << p;
-    if (MXQ_MX9_PACK_MIXED_FMA)
-      h[p] = q_pair_s16x2_bf16(w[p], __float_as_uint(t ? m1 : m0));
-    else
-      h[p] = q_pair_s16x2(w[p] << 16, w[p] & 0xFFFF0000u, t ? m1 : m0);
-  }
-  *q = make_uint4(__byte_perm(h[0], h[1], 0x6420), __byte_perm(h[2], h[3], 0x6420),
-                  __byte_perm(h[4], h[5], 0x6420), __byte_perm(h[6], h[7], 0x6420));
-  *eb_out = eb8;
-  *prime_out = bits;
-}
-
-template <bool kBF16>
-__global__ void __launch_bounds__(PackShape<kBF16>::kThreads, MXQ_MX9_PACK_CTAS_PER_SM)
-    mx9_pack_kernel(const uint8_t* __restrict__ x, int64_t nb, uint4* __restrict__ q,
+// kSplit: q [nb, 16] int8, max_exp [nb], prime [nb].  kRecMx9 / kRecMx6: out
+// is the packed tensor of nb records (16-byte aligned); q_or_rec points to it.
+template <bool kBF16, int kOut>
+__global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK_CTAS_PER_SM)
+    mx9_pack_kernel(const uint8_t* __restrict__ x, int64_t nb, uint8_t* __restrict__ q_or_rec,
                     uint8_t* __restrict__ max_exp, uint8_t* __restrict__ prime) {
-  using S = PackShape<kBF16>;
+  using S = PackShape<kBF16, kOut>;
+  using R = MxRule<kOut == kRecMx6 ? 3 : 6, kOut == kRecMx6 ? 15 : 127>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 127u) & ~127u;
@@ -304,43 +211,74 @@ __global__ void __launch_bounds__(PackShape<kBF16>::kThreads, MXQ_MX9_PACK_CTAS_
   }
 
   // -------------------------------------------------------------- consumers
+  // Record outputs: two staging buffers per warp, alternating over its runs;
+  // a whole run leaves with one bulk store issued by lane 0.
+  const uint32_t rec_stage = base + S::kOffRec + static_cast<uint32_t>(warp) * 2u * S::kRunBytes;
+  uint32_t runs = 0;
   for (int64_t i = 0; i < my; ++i) {
     const int s = static_cast<int>(i % S::kStages);
     const bool ok = mbar_wait_bounded(full(s), static_cast<uint32_t>((i / S::kStages) & 1),
                                       abort_flag, &g_mx9_status, MXQ_DEV_TIMEOUT);
-    if (!__all_sync(0xFFFFFFFFu, ok)) return;
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
     const int64_t blk0 = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * S::kBlocksPerStage;
 #pragma unroll
     for (int j = 0; j < S::kPerThread; ++j) {
       const int local = j * S::kConsumers + tid;
+      const int64_t run0 = blk0 + (local - lane);  // this warp's 32 consecutive blocks
+      if (run0 >= nb) break;                       // warp-uniform
       const int64_t blk = blk0 + local;
-      if (blk >= nb) break;
-      const uint32_t src = base + static_cast<uint32_t>(s) * S::kStageBytes + local * S::kBlockBytes;
-      uint4 qv;
-      uint32_t eb8, bits;
-      if (kBF16) {
-        const uint4 a = lds128(src), b = lds128(src + 16);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        pack_block_bf16(w, &qv, &eb8, &bits);
-      } else {
-        uint32_t f[16];
+      uint32_t h[8], eb8 = 0, bits = 0;
+      if (blk < nb) {
+        const uint32_t src =
+            base + static_cast<uint32_t>(s) * S::kStageBytes + local * S::kBlockBytes;
+        if (kBF16) {
+          const uint4 a = lds128(src), b = lds128(src + 16);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          R::block_bf16(w, h, &eb8, &bits);
+        } else {
+          uint32_t f[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 a = lds128(src + 16u * k);
-          f[4 * k] = a.x;
-          f[4 * k + 1] = a.y;
-          f[4 * k + 2] = a.z;
-          f[4 * k + 3] = a.w;
+          for (int k = 0; k < 4; ++k) {
+            const uint4 a = lds128(src + 16u * k);
+            f[4 * k] = a.x;
+            f[4 * k + 1] = a.y;
+            f[4 * k + 2] = a.z;
+            f[4 * k + 3] = a.w;
+          }
+          R::block_f32(f, h, &eb8, &bits);
         }
-        pack_block(f, &qv, &eb8, &bits);
       }
-      __stcs(q + blk, qv);
-      max_exp[blk] = static_cast<uint8_t>(eb8);
-      prime[blk] = static_cast<uint8_t>(bits);
+      if (kOut == kSplit) {
+        if (blk < nb) {
+          __stcs(reinterpret_cast<uint4*>(q_or_rec) + blk, pairs_to_bytes(h));
+          max_exp[blk] = static_cast<uint8_t>(eb8);
+          prime[blk] = static_cast<uint8_t>(bits);
+        }
+      } else {
+        const uint32_t buf = rec_stage + (runs & 1u) * S::kRunBytes;
+        ++runs;
+        if (lane == 0) bulk_wait_read<1>();  // the store that last read buf is done with it
+        __syncwarp();
+        if (blk < nb) stage_record<kOut>(buf + static_cast<uint32_t>(lane) * S::kRecord, eb8, bits, h);
+        const int64_t nvalid = nb - run0 < 32 ? nb - run0 : 32;
+        const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kRecord;
+        if (bytes % 16u == 0) {
+          fence_proxy_async_smem();  // staged records before the bulk store reads them
+          __syncwarp();
+          if (lane == 0) {
+            bulk_store(q_or_rec + run0 * S::kRecord, buf, bytes);
+            bulk_commit();
+          }
+        } else {  // the tensor's last, partial run
+          __syncwarp();
+          copy_records_out(q_or_rec + run0 * S::kRecord, buf, bytes, lane);
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(s));
   }
+  if (kOut != kSplit && lane == 0) bulk_wait_all<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -482,15 +420,15 @@ int check_dims(int dtype, int64_t rows, int64_t cols) {
   return MXQ_OK;
 }
 
-template <bool kBF16>
-cudaError_t launch_pack(const void* x, int64_t nb, int8_t* q, uint8_t* max_exp, uint8_t* prime,
-                        int sms, int dev, cudaStream_t stream) {
-  using S = PackShape<kBF16>;
+template <bool kBF16, int kOut>
+cudaError_t launch_pack(const void* x, int64_t nb, uint8_t* q_or_rec, uint8_t* max_exp,
+                        uint8_t* prime, int sms, int dev, cudaStream_t stream) {
+  using S = PackShape<kBF16, kOut>;
   static bool attr_done[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {  // benign race: setting the same attribute twice is harmless
     const cudaError_t e = cudaFuncSetAttribute(
-        mx9_pack_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+        mx9_pack_kernel<kBF16, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
@@ -501,8 +439,8 @@ cudaError_t launch_pack(const void* x, int64_t nb, int8_t* q, uint8_t* max_exp, 
   cfg.blockDim = dim3(S::kThreads);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, mx9_pack_kernel<kBF16>, static_cast<const uint8_t*>(x), nb,
-                            reinterpret_cast<uint4*>(q), max_exp, prime);
+  return cudaLaunchKernelEx(&cfg, mx9_pack_kernel<kBF16, kOut>, static_cast<const uint8_t*>(x),
+                            nb, q_or_rec, max_exp, prime);
 }
 
 }  // namespace
@@ -516,6 +454,24 @@ int mx9_status_read(unsigned int* out, bool clear) {
     if (cudaMemcpyToSymbol(g_mx9_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ECUDA;
   }
   return MXQ_OK;
+}
+
+// The packed-record form of the pack kernel for a contiguous tensor blocked
+// along its rows (x and packed 16-byte aligned, nb whole blocks); the caller
+// has checked the arguments.
+int launch_records_pack(const void* x, bool bf16, int fmt, int64_t nb, uint8_t* packed,
+                        cudaStream_t stream) {
+  int dev = 0;
+  const int sms = sm_count_current_device(&dev);
+  if (sms <= 0) return MXQ_ECUDA;
+  cudaError_t e;
+  if (fmt == MXQ_FMT_MX9)
+    e = bf16 ? launch_pack<true, kRecMx9>(x, nb, packed, nullptr, nullptr, sms, dev, stream)
+             : launch_pack<false, kRecMx9>(x, nb, packed, nullptr, nullptr, sms, dev, stream);
+  else
+    e = bf16 ? launch_pack<true, kRecMx6>(x, nb, packed, nullptr, nullptr, sms, dev, stream)
+             : launch_pack<false, kRecMx6>(x, nb, packed, nullptr, nullptr, sms, dev, stream);
+  return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 }  // namespace mxq
 
@@ -538,9 +494,10 @@ extern "C" int mx9_pack(const void* x, int dtype, int64_t rows, int64_t cols, in
   int dev = 0;
   const int sms = sm_count_current_device(&dev);
   if (sms <= 0) return MXQ_ECUDA;
-  const cudaError_t e = dtype == MXQ_F32
-                            ? launch_pack<false>(x, n / 16, q, max_exp, prime, sms, dev, stream)
-                            : launch_pack<true>(x, n / 16, q, max_exp, prime, sms, dev, stream);
+  uint8_t* qb = reinterpret_cast<uint8_t*>(q);
+  const cudaError_t e =
+      dtype == MXQ_F32 ? launch_pack<false, kSplit>(x, n / 16, qb, max_exp, prime, sms, dev, stream)
+                       : launch_pack<true, kSplit>(x, n / 16, qb, max_exp, prime, sms, dev, stream);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 

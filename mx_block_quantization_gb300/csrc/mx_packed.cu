@@ -12,14 +12,21 @@
 // 5-bit two's-complement codes, element i at bits 5i..5i+4 of the 10 data
 // bytes read as one little-endian number.
 //
-// One thread owns one block.  Along axis 1 (a row) a warp's 32 blocks are
-// consecutive records: the warp stages them in shared memory and moves them
-// with 16-byte coalesced copies; along axis 0 (a column) the lanes of a warp
-// take neighbouring columns, so every element load and store is coalesced and
-// each record is written with its own narrow stores.
+// A contiguous tensor blocked along its rows (the common case) is a flat run
+// of whole blocks: packing goes through the TMA-fed pack kernel of mx9.cu in
+// its record form, and unpacking through mx_unpack_records_kernel below, where
+// a warp copies 32 records into shared memory with 16-byte loads and each lane
+// then writes 16 output bytes.  Every other geometry (blocks along columns,
+// strided rows, partial blocks) takes the generic kernels: one thread owns one
+// block; along axis 1 (a row) a warp's 32 blocks are consecutive records,
+// staged in shared memory and moved with 16-byte coalesced copies; along axis
+// 0 (a column) the lanes of a warp take neighbouring columns, so every element
+// load and store is coalesced and each record is written with its own narrow
+// stores.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mx_block.cuh"
 #include "mxq.h"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
@@ -391,6 +398,108 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Exact float of a small integer q (|q| < 2^22) without a conversion
+// instruction: the bits of 1.5 * 2^23 + q, minus 1.5 * 2^23.
+__device__ __forceinline__ float small_int_float(int32_t q) {
+  float r;
+  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(__int_as_float(0x4B400000 + q)), "f"(-12582912.0f));
+  return r;
+}
+
+// Unpack of a contiguous tensor blocked along its rows: nb records, the
+// output is nb * 16 elements.  Each warp takes runs of 32 records: copies them
+// into shared memory with 16-byte loads, then each lane rebuilds 16 output
+// bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp cover
+// 512 contiguous bytes.  packed and y are 16-byte aligned.
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb,
+                             uint8_t* __restrict__ y) {
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  constexpr int kElems = kBF16 ? 8 : 4;  // elements per 16 output bytes
+  constexpr int kParts = 16 / kElems;    // output units per block
+  __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t st = smem_u32(stage[warp]);
+  const int64_t nruns = (nb + 31) / 32;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t run = static_cast<int64_t>(blockIdx.x) * kWarps + warp; run < nruns; run += wstride) {
+    const int64_t r0 = run * 32;
+    const int nvalid = static_cast<int>(nb - r0 < 32 ? nb - r0 : 32);
+    // copy in: 16-byte units, then 2-byte pieces
+    const uint8_t* src = packed + r0 * RB;
+    const int bytes = nvalid * RB, n16 = bytes >> 4;
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+      sts128(st + 16u * i, v.x, v.y, v.z, v.w);
+    }
+    for (int i = n16 * 8 + lane; i < (bytes >> 1); i += 32) {
+      const uint32_t v = __ldcs(reinterpret_cast<const uint16_t*>(src) + i);
+      asm volatile("st.shared.u16 [%0], %1;" ::"r"(st + 2u * i), "r"(v) : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kParts; ++j) {
+      const int u = j * 32 + lane;  // output unit of this run
+      const int r = u / kParts, part = u % kParts;
+      if (r >= nvalid) continue;
+      const uint32_t rec = st + static_cast<uint32_t>(r) * RB;
+      uint32_t head, code[kElems];
+      if (kFmt == MXQ_FMT_MX9) {
+        head = lds_u16(rec);
+#pragma unroll
+        for (int k = 0; k < kElems / 2; ++k) {
+          const uint32_t two = lds_u16(rec + 2u + static_cast<uint32_t>(part * kElems + 2 * k));
+          code[2 * k] = two & 0xFFu;
+          code[2 * k + 1] = two >> 8;
+        }
+      } else {
+        const uint32_t w0 = lds32(rec), w1 = lds32(rec + 4u), w2 = lds32(rec + 8u);
+        head = w0 & 0xFFFFu;
+        // data bits: d_lo = bits 0..63, d_hi = bits 64..79
+        const uint64_t d_lo = static_cast<uint64_t>(w0 >> 16) | (static_cast<uint64_t>(w1) << 16) |
+                              (static_cast<uint64_t>(w2) << 48);
+        const uint32_t d_hi = w2 >> 16;
+        const int b0 = 5 * part * kElems;  // first bit of this unit's codes
+        const uint64_t d = b0 == 0 ? d_lo : (d_lo >> b0) | (static_cast<uint64_t>(d_hi) << (64 - b0));
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) code[k] = static_cast<uint32_t>(d >> (5 * k)) & 0x1Fu;
+      }
+      const int eb8 = static_cast<int>(head & 0xFFu);
+      const uint32_t bits = head >> 8;
+      float v[kElems];
+#pragma unroll
+      for (int k = 0; k < kElems; ++k) {
+        const int pair = (part * kElems + k) >> 1;
+        const int t = static_cast<int>((bits >> pair) & 1u);
+        // 2^k, k = max(E - off - t, -126): exponent field max(eb8 - off - t, 1)
+        const float sc = __uint_as_float(
+            static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset - t, 1)) << 23);
+        const int q = kFmt == MXQ_FMT_MX9 ? static_cast<int>(static_cast<int8_t>(code[k]))
+                                          : static_cast<int>(code[k] << 27) >> 27;
+        v[k] = fmul_rn_noftz(small_int_float(q), sc);
+      }
+      const int64_t unit = (r0 + r) * kParts + part;  // 16-byte output unit
+      if (kBF16) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          o[k] = __byte_perm(__float_as_uint(v[2 * k]), __float_as_uint(v[2 * k + 1]), 0x7632);
+        __stcs(reinterpret_cast<uint4*>(y) + unit, make_uint4(o[0], o[1], o[2], o[3]));
+      } else {
+        __stcs(reinterpret_cast<float4*>(y) + unit, make_float4(v[0], v[1], v[2], v[3]));
+      }
+    }
+    __syncwarp();
+  }
+}
+
 int check_args(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, int axis, int fmt,
                const void* packed, int64_t* nb_out) {
   if (dtype != MXQ_F32 && dtype != MXQ_BF16) return MXQ_EBADDTYPE;
@@ -412,6 +521,14 @@ int check_args(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
   return MXQ_OK;
 }
 
+// A tensor blocked along its rows whose rows follow each other with no gap and
+// hold whole blocks: a flat run of 16-element blocks.
+bool flat_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, int axis) {
+  return axis == 1 && cols % 16 == 0 && (ld == cols || rows == 1) && aligned_to(x, 16);
+}
+
+// One thread per work item (capped at a full wave of 8 blocks per SM); the
+// records unpack takes one warp per 32 records, the same count per block.
 template <typename Kernel, typename... Args>
 int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
   const int sms = sm_count_current_device(nullptr);
@@ -432,6 +549,8 @@ extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t co
   int64_t nb = 0;
   const int rc = check_args(x, dtype, rows, cols, ld, axis, fmt, packed, &nb);
   if (rc != MXQ_OK || nb == 0) return rc;
+  if (flat_rows(x, rows, cols, ld, axis) && aligned_to(packed, 16))
+    return launch_records_pack(x, dtype == MXQ_BF16, fmt, nb, packed, stream);
   const Geometry g{rows, cols, ld, axis};
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
   const bool vec_rows = aligned_to(x, 16) && (ld * esize) % 16 == 0;
@@ -451,11 +570,20 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   int64_t nb = 0;
   const int rc = check_args(y, dtype, rows, cols, ld, axis, fmt, packed, &nb);
   if (rc != MXQ_OK || nb == 0) return rc;
+  uint8_t* yb = static_cast<uint8_t*>(y);
+  if (flat_rows(y, rows, cols, ld, axis) && aligned_to(packed, 16)) {
+    if (dtype == MXQ_F32)
+      return fmt == MXQ_FMT_MX9
+                 ? launch(mx_unpack_records_kernel<false, MXQ_FMT_MX9>, nb, stream, packed, nb, yb)
+                 : launch(mx_unpack_records_kernel<false, MXQ_FMT_MX6>, nb, stream, packed, nb, yb);
+    return fmt == MXQ_FMT_MX9
+               ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, nb, stream, packed, nb, yb)
+               : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, nb, stream, packed, nb, yb);
+  }
   const Geometry g{rows, cols, ld, axis};
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
   const bool vec_rows = aligned_to(y, 16) && (ld * esize) % 16 == 0;
   const bool pal = aligned_to(packed, 16);
-  uint8_t* yb = static_cast<uint8_t*>(y);
   if (dtype == MXQ_F32)
     return fmt == MXQ_FMT_MX9
                ? launch(mx_unpack_packed_kernel<false, MXQ_FMT_MX9>, nb, stream, packed, g, vec_rows, pal, yb)

@@ -53,7 +53,9 @@ def _check(x_full: np.ndarray, cols: int, fmt: int, axis: int, tag: str):
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("axis", [0, 1])
 @pytest.mark.parametrize("rows,cols,ld", [(64, 256, 256), (20, 37, 37), (48, 80, 112),
-                                          (33, 16, 24), (1, 15, 15), (257, 129, 136)])
+                                          (33, 16, 24), (1, 15, 15), (257, 129, 136),
+                                          (3, 16, 16), (7, 48, 48), (1000, 160, 160),
+                                          (1, 4096, 4096), (129, 2048, 2048)])
 def test_packed_shapes(fmt, dt, axis, rows, cols, ld):
     x = np.zeros((rows, ld), np.float32)
     x[:, :cols] = W.mx9_outliers(rows, cols, seed=rows * cols + axis, zero_blocks=0, tiny_blocks=0)
