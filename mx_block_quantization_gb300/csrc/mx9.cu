@@ -45,6 +45,18 @@ using namespace mxq;
 #ifndef MXQ_MX9_PACK_BF16_RING_KB
 #define MXQ_MX9_PACK_BF16_RING_KB 48
 #endif
+#ifndef MXQ_MX9_REC_F32_WARPS
+#define MXQ_MX9_REC_F32_WARPS 12
+#endif
+#ifndef MXQ_MX9_REC_F32_RING_KB
+#define MXQ_MX9_REC_F32_RING_KB 96
+#endif
+#ifndef MXQ_MX9_REC_BF16_WARPS
+#define MXQ_MX9_REC_BF16_WARPS 16
+#endif
+#ifndef MXQ_MX9_REC_BF16_RING_KB
+#define MXQ_MX9_REC_BF16_RING_KB 64
+#endif
 #ifndef MXQ_MX9_PACK_CTAS_PER_SM
 #define MXQ_MX9_PACK_CTAS_PER_SM 2
 #endif
@@ -79,10 +91,13 @@ enum PackOut { kSplit = 0, kRecMx9 = MXQ_FMT_MX9, kRecMx6 = MXQ_FMT_MX6 };
 // Pack kernel shape per input type: consumer warps (kPerThread 16-element
 // blocks per consumer thread and stage), one producer warp, a ring of stages,
 // and for record outputs a per-warp staging area of 32 records.  Rings deeper
-// than these measured slower.
+// than these measured slower; the record forms, with more instructions per
+// block, measured faster with more warps.
 template <bool kBF16, int kOut>
 struct PackShape {
-  static constexpr int kWarps = kBF16 ? MXQ_MX9_PACK_BF16_WARPS : MXQ_MX9_PACK_F32_WARPS;
+  static constexpr int kWarps =
+      kOut == kSplit ? (kBF16 ? MXQ_MX9_PACK_BF16_WARPS : MXQ_MX9_PACK_F32_WARPS)
+                     : (kBF16 ? MXQ_MX9_REC_BF16_WARPS : MXQ_MX9_REC_F32_WARPS);
   static constexpr int kPerThread = kBF16 ? MXQ_MX9_PACK_BF16_PER_THREAD : MXQ_MX9_PACK_F32_PER_THREAD;
   static constexpr int kThreads = (kWarps + 1) * 32;
   static constexpr int kConsumers = kWarps * 32;
@@ -90,7 +105,9 @@ struct PackShape {
   static constexpr uint32_t kBlockBytes = kBF16 ? 32u : 64u;  // 16 elements
   static constexpr uint32_t kStageBytes = kBlocksPerStage * kBlockBytes;
   static constexpr uint32_t kRingBytes =
-      (kBF16 ? MXQ_MX9_PACK_BF16_RING_KB : MXQ_MX9_PACK_F32_RING_KB) * 1024u;
+      (kOut == kSplit ? (kBF16 ? MXQ_MX9_PACK_BF16_RING_KB : MXQ_MX9_PACK_F32_RING_KB)
+                      : (kBF16 ? MXQ_MX9_REC_BF16_RING_KB : MXQ_MX9_REC_F32_RING_KB)) *
+      1024u;
   static constexpr int kStages = static_cast<int>(kRingBytes / kStageBytes);
   static constexpr uint32_t kRecord =
       kOut == kRecMx9 ? MXQ_MX9_RECORD_BYTES : kOut == kRecMx6 ? MXQ_MX6_RECORD_BYTES : 0u;
