@@ -412,11 +412,17 @@ __device__ __forceinline__ float small_int_float(int32_t q) {
   return r;
 }
 
+#ifndef MXQ_REC_UNPACK_RUNS
+#define MXQ_REC_UNPACK_RUNS 4
+#endif
+constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight per warp
+
 // Unpack of a contiguous tensor blocked along its rows: nb records, the
-// output is nb * 16 elements.  Each warp takes runs of 32 records: copies them
-// into shared memory with 16-byte loads, then each lane rebuilds 16 output
-// bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp cover
-// 512 contiguous bytes.  packed and y are 16-byte aligned.
+// output is nb * 16 elements.  Each warp takes kRecRuns consecutive runs of 32
+// records at a time: copies them into shared memory with 16-byte loads (all
+// loads issued before the first shared store), then each lane rebuilds 16
+// output bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp
+// cover 512 contiguous bytes.  packed and y are 16-byte aligned.
 template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb,
@@ -424,29 +430,39 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int kElems = kBF16 ? 8 : 4;  // elements per 16 output bytes
   constexpr int kParts = 16 / kElems;    // output units per block
-  __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
+  constexpr int kGroup = 32 * kRecRuns;  // records per warp iteration
+  constexpr int kLoads = (kGroup * RB / 16 + 31) / 32;  // 16-byte loads per lane
+  __shared__ __align__(16) uint8_t stage[kWarps][kGroup * kMaxRecord];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t st = smem_u32(stage[warp]);
-  const int64_t nruns = (nb + 31) / 32;
+  const int64_t ngroups = (nb + kGroup - 1) / kGroup;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kWarps;
-  for (int64_t run = static_cast<int64_t>(blockIdx.x) * kWarps + warp; run < nruns; run += wstride) {
-    const int64_t r0 = run * 32;
-    const int nvalid = static_cast<int>(nb - r0 < 32 ? nb - r0 : 32);
+  for (int64_t grp = static_cast<int64_t>(blockIdx.x) * kWarps + warp; grp < ngroups;
+       grp += wstride) {
+    const int64_t r0 = grp * kGroup;
+    const int nvalid = static_cast<int>(nb - r0 < kGroup ? nb - r0 : kGroup);
     // copy in: 16-byte units, then 2-byte pieces
     const uint8_t* src = packed + r0 * RB;
     const int bytes = nvalid * RB, n16 = bytes >> 4;
-    for (int i = lane; i < n16; i += 32) {
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src) + i);
-      sts128(st + 16u * i, v.x, v.y, v.z, v.w);
+    uint4 v[kLoads];
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+      const int i = lane + 32 * k;
+      if (i < n16) v[k] = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+    }
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+      const int i = lane + 32 * k;
+      if (i < n16) sts128(st + 16u * i, v[k].x, v[k].y, v[k].z, v[k].w);
     }
     for (int i = n16 * 8 + lane; i < (bytes >> 1); i += 32) {
-      const uint32_t v = __ldcs(reinterpret_cast<const uint16_t*>(src) + i);
-      asm volatile("st.shared.u16 [%0], %1;" ::"r"(st + 2u * i), "r"(v) : "memory");
+      const uint32_t h = __ldcs(reinterpret_cast<const uint16_t*>(src) + i);
+      asm volatile("st.shared.u16 [%0], %1;" ::"r"(st + 2u * i), "r"(h) : "memory");
     }
     __syncwarp();
 #pragma unroll
-    for (int j = 0; j < kParts; ++j) {
-      const int u = j * 32 + lane;  // output unit of this run
+    for (int j = 0; j < kParts * kRecRuns; ++j) {
+      const int u = j * 32 + lane;  // output unit of this group
       const int r = u / kParts, part = u % kParts;
       if (r >= nvalid) continue;
       const uint32_t rec = st + static_cast<uint32_t>(r) * RB;
@@ -473,7 +489,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       const int eb8 = static_cast<int>(head & 0xFFu);
       const uint32_t bits = head >> 8;
-      float v[kElems];
+      float val[kElems];
 #pragma unroll
       for (int k = 0; k < kElems; ++k) {
         const int pair = (part * kElems + k) >> 1;
@@ -483,17 +499,17 @@ __global__ void __launch_bounds__(kThreads)
             static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset - t, 1)) << 23);
         const int q = kFmt == MXQ_FMT_MX9 ? static_cast<int>(static_cast<int8_t>(code[k]))
                                           : static_cast<int>(code[k] << 27) >> 27;
-        v[k] = fmul_rn_noftz(small_int_float(q), sc);
+        val[k] = fmul_rn_noftz(small_int_float(q), sc);
       }
       const int64_t unit = (r0 + r) * kParts + part;  // 16-byte output unit
       if (kBF16) {
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          o[k] = __byte_perm(__float_as_uint(v[2 * k]), __float_as_uint(v[2 * k + 1]), 0x7632);
+          o[k] = __byte_perm(__float_as_uint(val[2 * k]), __float_as_uint(val[2 * k + 1]), 0x7632);
         __stcs(reinterpret_cast<uint4*>(y) + unit, make_uint4(o[0], o[1], o[2], o[3]));
       } else {
-        __stcs(reinterpret_cast<float4*>(y) + unit, make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(reinterpret_cast<float4*>(y) + unit, make_float4(val[0], val[1], val[2], val[3]));
       }
     }
     __syncwarp();
@@ -527,8 +543,7 @@ bool flat_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, int axis) 
   return axis == 1 && cols % 16 == 0 && (ld == cols || rows == 1) && aligned_to(x, 16);
 }
 
-// One thread per work item (capped at a full wave of 8 blocks per SM); the
-// records unpack takes one warp per 32 records, the same count per block.
+// One thread per work item (capped at a full wave of 8 blocks per SM).
 template <typename Kernel, typename... Args>
 int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
   const int sms = sm_count_current_device(nullptr);
@@ -574,11 +589,11 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   if (flat_rows(y, rows, cols, ld, axis) && aligned_to(packed, 16)) {
     if (dtype == MXQ_F32)
       return fmt == MXQ_FMT_MX9
-                 ? launch(mx_unpack_records_kernel<false, MXQ_FMT_MX9>, nb, stream, packed, nb, yb)
-                 : launch(mx_unpack_records_kernel<false, MXQ_FMT_MX6>, nb, stream, packed, nb, yb);
+                 ? launch(mx_unpack_records_kernel<false, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb)
+                 : launch(mx_unpack_records_kernel<false, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb);
     return fmt == MXQ_FMT_MX9
-               ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, nb, stream, packed, nb, yb)
-               : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, nb, stream, packed, nb, yb);
+               ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb)
+               : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb);
   }
   const Geometry g{rows, cols, ld, axis};
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
