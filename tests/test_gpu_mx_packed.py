@@ -98,3 +98,35 @@ def test_packed_rejections():
         mxq.mx_pack_packed(torch.zeros((4, 16), device="cuda"), 7, 1)       # unknown format
     with pytest.raises(ValueError):
         mxq.mx_pack_packed(torch.zeros((4, 16), device="cuda").t(), mxq.FMT_MX9, 1)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("x_off,p_off", [(1, 0), (0, 1)])
+def test_packed_offsets_below_16_bytes(fmt, dt, x_off, p_off):
+    """Element pointers one element off 16 bytes, or records at the smallest
+    allowed offset (2 bytes for MX9, 4 for MX6): the contiguous row-blocked
+    case then runs without its 16-byte vector paths and gives the same bytes."""
+    rows, cols = 64, 512
+    x = W.mx9_outliers(rows, cols, seed=21, zero_blocks=0, tiny_blocks=0)
+    if dt == "bf16":
+        x = W.f32_to_bf16_bits(x)
+    rb, nb = mxq.RECORD_BYTES[fmt], rows * cols // 16
+    want = oracle.mx_pack(x, fmt, axis=1)
+    flat = np.concatenate([np.zeros(1, x.dtype), x.reshape(-1)])
+    xd = _dev(flat)[x_off:x_off + rows * cols].view(rows, cols)
+    poff = (2 if fmt == mxq.FMT_MX9 else 4) * p_off
+    big = torch.zeros(nb * rb + 16, dtype=torch.uint8, device="cuda")
+    pk = big[poff:poff + nb * rb]
+    mxq.mx_pack_packed(xd, fmt, 1, out=pk)
+    torch.cuda.synchronize()
+    assert_bytes_equal(pk.cpu().numpy().reshape(nb, rb), want, f"fmt{fmt} {dt} pack offsets")
+    is_bf16 = dt == "bf16"
+    fill = np.full(rows * cols + 1, 0x5A5A if is_bf16 else np.float32(-3.25), x.dtype)
+    yd_big = _dev(fill)
+    yd = yd_big[x_off:x_off + rows * cols].view(rows, cols)
+    mxq.mx_unpack_packed(pk, fmt, yd, 1)
+    ref = oracle.mx_unpack(want, fmt, rows, cols, "bf16" if is_bf16 else "f32", axis=1)
+    torch.cuda.synchronize()
+    got = yd.cpu().view(torch.int16 if is_bf16 else torch.int32).numpy()
+    assert_bytes_equal(got.view(np.uint8), ref.view(np.uint8), f"fmt{fmt} {dt} unpack offsets")
