@@ -602,13 +602,13 @@ def run_case(args):
         # the single packed tensor of MX9 (--fmt 9) or MX6 (--fmt 6) records, rows blocked
         tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
         xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
-        rec = mxq.mx_pack_packed(xm, args.fmt, 1)
+        rec = mxq.mx_pack_packed(xm, args.fmt, args.axis)
         y = torch.empty_like(xm)
         for _ in range(args.warmup):
             if args.case.startswith("rec_pack"):
-                mxq.mx_pack_packed(xm, args.fmt, 1, out=rec)
+                mxq.mx_pack_packed(xm, args.fmt, args.axis, out=rec)
             else:
-                mxq.mx_unpack_packed(rec, args.fmt, y, 1)
+                mxq.mx_unpack_packed(rec, args.fmt, y, args.axis)
     else:
         tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
         xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
@@ -621,7 +621,7 @@ def run_case(args):
     torch.cuda.synchronize()
     assert mxq.device_status(clear=True) == 0
     print(json.dumps({"case": args.case, "shape": [M, N], "launches": args.warmup,
-                      **({"fmt": args.fmt} if args.case.startswith("rec_") else {})}))
+                      **({"fmt": args.fmt, "axis": args.axis} if args.case.startswith("rec_") else {})}))
     return 0
 
 
@@ -643,6 +643,8 @@ def main(argv=None):
     ap.add_argument("--shape", default="16384x7168")
     ap.add_argument("--fmt", type=int, choices=[9, 6], default=9,
                     help="with --case rec_*: MX9 or MX6 records")
+    ap.add_argument("--axis", type=int, choices=[0, 1], default=1,
+                    help="with --case rec_*: blocks along columns (0) or rows (1)")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --case dual: that many K-groups and a 1/8 uncovered tail")
     args = ap.parse_args(argv)

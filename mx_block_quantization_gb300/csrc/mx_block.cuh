@@ -18,6 +18,7 @@
 
 #include <stdint.h>
 
+#include "mxq.h"
 #include "mxq_device.cuh"
 
 namespace mxq {
@@ -171,6 +172,53 @@ __device__ __forceinline__ void pairs_to_codes5(const uint32_t* h, uint32_t* lo,
   *lo = c[0] | (c[1] << 10) | (c[2] << 20) | (c[3] << 30);
   *mid = (c[3] >> 2) | (c[4] << 8) | (c[5] << 18) | (c[6] << 28);
   *hi = (c[6] >> 4) | (c[7] << 6);
+}
+
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Copy a warp's staged records (16-byte aligned on both sides, an even
+// number of bytes) to global memory: 16-byte units, then 2-byte pieces.
+__device__ __forceinline__ void copy_records_out(uint8_t* g, uint32_t s, uint32_t bytes, int lane) {
+  const uint32_t n16 = bytes >> 4;
+  for (uint32_t i = lane; i < n16; i += 32) __stcs(reinterpret_cast<uint4*>(g) + i, lds128(s + 16u * i));
+  const uint32_t h0 = n16 * 8u, nh = bytes >> 1;
+  for (uint32_t i = h0 + lane; i < nh; i += 32) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(s + 2u * i));
+    reinterpret_cast<uint16_t*>(g)[i] = static_cast<uint16_t>(v);
+  }
+}
+
+// Stage one block record at shared address a: [exponent, prime, data].
+template <int kFmt>
+__device__ __forceinline__ void stage_record(uint32_t a, uint32_t eb8, uint32_t bits,
+                                             const uint32_t* h) {
+  const uint32_t head = eb8 | (bits << 8);
+  if (kFmt == MXQ_FMT_MX9) {  // 18 bytes at a 2-byte aligned address
+    const uint4 q = pairs_to_bytes(h);
+    const uint32_t w[5] = {head | (q.x << 16), __byte_perm(q.x, q.y, 0x5432),
+                           __byte_perm(q.y, q.z, 0x5432), __byte_perm(q.z, q.w, 0x5432), q.w >> 16};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      sts16(a + 4u * k, w[k] & 0xFFFFu);
+      sts16(a + 4u * k + 2u, w[k] >> 16);
+    }
+    sts16(a + 16u, w[4]);
+  } else {  // MX6: 12 bytes at a 4-byte aligned address
+    uint32_t lo, mid, hi;
+    pairs_to_codes5(h, &lo, &mid, &hi);
+    sts32(a, head | (lo << 16));
+    sts32(a + 4u, (lo >> 16) | (mid << 16));
+    sts32(a + 8u, (mid >> 16) | (hi << 16));
+  }
 }
 
 }  // namespace mxq

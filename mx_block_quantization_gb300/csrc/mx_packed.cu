@@ -516,6 +516,467 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ---------------------------------------------------------------------------
+// blocks along columns (axis 0): a shared-memory transpose
+// ---------------------------------------------------------------------------
+// A CTA takes a tile of kColTileRows rows (32 blocks) x 32 columns: rows are
+// read (or written) with coalesced warp accesses into an XOR-swizzled tile,
+// element (r, c) at r * 32 + (c ^ (r / 16 % 32)), so that a row's 32 columns
+// and a column's 32 blocks (one per lane) each fall in 32 different banks.
+// The 32 blocks of one column in a tile are 32 consecutive records: a warp
+// stages them and moves them as one run.  Tiles are visited across a band of
+// rows first, so the CTAs running at one time share the DRAM pages of the
+// same rows.
+constexpr int kColTileRows = 512;
+constexpr int kColTileCols = 32;
+
+template <bool kBF16>
+struct ColTile {
+  static constexpr uint32_t kElem = kBF16 ? 2u : 4u;
+  static constexpr uint32_t kTileBytes = kColTileRows * kColTileCols * kElem;
+  static constexpr uint32_t kSmemBytes = kTileBytes + kWarps * 32u * kMaxRecord;
+  // unpack: records of all kColsPerWarp columns of a warp staged at once
+  static constexpr int kColsPerWarp = kColTileCols / kWarps;
+  static constexpr uint32_t kUnpackSmemBytes = kTileBytes + kWarps * kColsPerWarp * 32u * kMaxRecord;
+};
+
+__device__ __forceinline__ uint32_t col_swizzle(int r, int c) {
+  return static_cast<uint32_t>(r * kColTileCols + (c ^ ((r >> 4) & 31)));
+}
+
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_pack_cols_kernel(const uint8_t* __restrict__ x, Geometry g, bool packed_aligned,
+                        uint8_t* __restrict__ packed) {
+  using T = ColTile<kBF16>;
+  using R = MxRule<Fmt<kFmt>::kOffset, Fmt<kFmt>::kQMax>;
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t tile = smem_u32(smem);
+  uint8_t* stage = smem + T::kTileBytes + warp * 32 * kMaxRecord;
+  const int64_t nbl = (g.rows + 15) / 16;  // blocks per column
+  const int64_t tiles_r = (g.rows + kColTileRows - 1) / kColTileRows;
+  const int64_t tiles_c = (g.cols + kColTileCols - 1) / kColTileCols;
+  for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int64_t tc = t % tiles_c, tr = t / tiles_c;  // across a row band first
+    const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
+    const bool col_ok = c0 + lane < g.cols;
+#pragma unroll 8
+    for (int r = warp; r < kColTileRows; r += kWarps) {
+      const int64_t row = r0 + r;
+      const uint32_t v = (col_ok && row < g.rows) ? load_bits<kBF16>(x, row * g.ld + c0 + lane) : 0u;
+      if (kBF16)
+        sts16(tile + 2u * col_swizzle(r, lane), v >> 16);
+      else
+        sts32(tile + 4u * col_swizzle(r, lane), v);
+    }
+    __syncthreads();
+    const int nvalid = static_cast<int>(nbl - tr * 32 < 32 ? nbl - tr * 32 : 32);
+    for (int cc = warp; cc < kColTileCols && c0 + cc < g.cols; cc += kWarps) {
+      const int j = lane;  // block j of this tile, in column c0 + cc
+      if (j < nvalid) {
+        uint32_t h[8], eb8, bits;
+        if (kBF16) {
+          uint32_t w[8];
+#pragma unroll
+          for (int p = 0; p < 8; ++p)
+            w[p] = lds16(tile + 2u * col_swizzle(16 * j + 2 * p, cc)) |
+                   (lds16(tile + 2u * col_swizzle(16 * j + 2 * p + 1, cc)) << 16);
+          R::block_bf16(w, h, &eb8, &bits);
+        } else {
+          uint32_t f[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) f[i] = lds32(tile + 4u * col_swizzle(16 * j + i, cc));
+          R::block_f32(f, h, &eb8, &bits);
+        }
+        stage_record<kFmt>(smem_u32(stage) + static_cast<uint32_t>(j) * RB, eb8, bits, h);
+      }
+      __syncwarp();
+      const int64_t b0 = (c0 + cc) * nbl + tr * 32;
+      warp_copy_out(packed + b0 * RB, stage, nvalid * RB,
+                    packed_aligned && ((b0 * RB) & 15) == 0, lane);
+      __syncwarp();
+    }
+    __syncthreads();
+  }
+}
+
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_unpack_cols_kernel(const uint8_t* __restrict__ packed, Geometry g, bool packed_aligned,
+                          uint8_t* __restrict__ y) {
+  using T = ColTile<kBF16>;
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  constexpr int kRun = 32 * kMaxRecord;  // staging bytes per column
+  constexpr int kLoads = (32 * RB / 16 + 31) / 32;  // 16-byte loads per lane and column
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t tile = smem_u32(smem);
+  uint8_t* stage = smem + T::kTileBytes + warp * T::kColsPerWarp * kRun;
+  const int64_t nbl = (g.rows + 15) / 16;
+  const int64_t tiles_r = (g.rows + kColTileRows - 1) / kColTileRows;
+  const int64_t tiles_c = (g.cols + kColTileCols - 1) / kColTileCols;
+  for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int64_t tc = t % tiles_c, tr = t / tiles_c;  // across a row band first
+    const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
+    const int nvalid = static_cast<int>(nbl - tr * 32 < 32 ? nbl - tr * 32 : 32);
+    // copy in the records of this warp's columns (cc = warp + kWarps * k): with
+    // 16-byte loads, all issued before the first shared store, when aligned
+    const int bytes = nvalid * RB;
+    const bool fast = packed_aligned && ((nbl * RB) & 15) == 0 && ((tr * 32 * RB) & 15) == 0;
+    if (fast) {
+      uint4 v[T::kColsPerWarp][kLoads];
+#pragma unroll
+      for (int k = 0; k < T::kColsPerWarp; ++k) {
+        const int64_t col = c0 + warp + kWarps * k;
+        const uint4* src = reinterpret_cast<const uint4*>(packed + (col * nbl + tr * 32) * RB);
+#pragma unroll
+        for (int l = 0; l < kLoads; ++l) {
+          const int i = lane + 32 * l;
+          if (col < g.cols && i < (bytes >> 4)) v[k][l] = __ldcs(src + i);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < T::kColsPerWarp; ++k) {
+        const uint32_t st = smem_u32(stage + k * kRun);
+#pragma unroll
+        for (int l = 0; l < kLoads; ++l) {
+          const int i = lane + 32 * l;
+          if (c0 + warp + kWarps * k < g.cols && i < (bytes >> 4))
+            sts128(st + 16u * i, v[k][l].x, v[k][l].y, v[k][l].z, v[k][l].w);
+        }
+      }
+      // bytes % 16 != 0 only for a column's last, partial run
+      for (int k = 0; k < T::kColsPerWarp; ++k) {
+        const int64_t col = c0 + warp + kWarps * k;
+        if (col >= g.cols) break;
+        const uint8_t* src = packed + (col * nbl + tr * 32) * RB;
+        for (int i = (bytes & ~15) + lane; i < bytes; i += 32) stage[k * kRun + i] = __ldg(src + i);
+      }
+    } else {
+      for (int k = 0; k < T::kColsPerWarp; ++k) {
+        const int64_t col = c0 + warp + kWarps * k;
+        if (col >= g.cols) break;
+        warp_copy_in(stage + k * kRun, packed + (col * nbl + tr * 32) * RB, bytes, false, lane);
+      }
+    }
+    __syncwarp();
+    for (int k = 0; k < T::kColsPerWarp; ++k) {
+      const int cc = warp + kWarps * k;
+      if (c0 + cc >= g.cols) break;
+      const int j = lane;
+      if (j < nvalid) {
+        const uint32_t rec = smem_u32(stage + k * kRun) + static_cast<uint32_t>(j) * RB;
+        uint32_t w[5];
+#pragma unroll
+        for (int q = 0; q < (RB + 3) / 4; ++q)
+          w[q] = lds16(rec + 4u * q) | (4 * q + 2 < RB ? lds16(rec + 4u * q + 2u) << 16 : 0u);
+        uint32_t eb8, bits;
+        int qv[16];
+        decode_record<kFmt>(w, &eb8, &bits, qv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int tbit = static_cast<int>((bits >> (i / 2)) & 1u);
+          const int kf = max(static_cast<int>(eb8) - Fmt<kFmt>::kOffset - tbit, 1);
+          const float v = fmul_rn_noftz(static_cast<float>(qv[i]),
+                                        __uint_as_float(static_cast<uint32_t>(kf) << 23));
+          if (kBF16)
+            sts16(tile + 2u * col_swizzle(16 * j + i, cc), __float_as_uint(v) >> 16);
+          else
+            sts32(tile + 4u * col_swizzle(16 * j + i, cc), __float_as_uint(v));
+        }
+      }
+    }
+    __syncthreads();
+    const bool col_ok = c0 + lane < g.cols;
+#pragma unroll 8
+    for (int r = warp; r < kColTileRows; r += kWarps) {
+      const int64_t row = r0 + r;
+      if (!col_ok || row >= g.rows) continue;
+      const int64_t idx = row * g.ld + c0 + lane;
+      if (kBF16)
+        reinterpret_cast<uint16_t*>(y)[idx] = static_cast<uint16_t>(lds16(tile + 2u * col_swizzle(r, lane)));
+      else
+        reinterpret_cast<uint32_t*>(y)[idx] = lds32(tile + 4u * col_swizzle(r, lane));
+    }
+    __syncthreads();
+  }
+}
+
+// Vector form of the column tiles, for tensors whose rows can be moved in
+// 16-byte pieces (16-byte aligned base, row pitch a multiple of 16 bytes,
+// columns a multiple of a piece).  A tile is 128 rows (8 blocks) x 32 pieces
+// (128 fp32 or 256 bf16 columns, 64 KB): rows are loaded and stored one
+// 16-byte piece per lane, piece p of row r sitting at position p ^ (r / 16 % 8)
+// of the row.  A lane then takes one block j (rows 16j..16j+15) of one word
+// column (one fp32 column, two bf16 columns) of piece group pg: its 16 words
+// sit at positions pg ^ j, so the 32 lanes (8 blocks x 4 words of a piece)
+// read 32 different banks.  Each warp step covers 4 pieces' worth of columns x
+// 8 blocks; the 8 records of one column form one run.
+constexpr int kVecTileRows = 128;
+constexpr int kVecPieces = 32;                        // 16-byte pieces per tile row
+constexpr uint32_t kVecTileBytes = kVecTileRows * kVecPieces * 16u;
+
+template <bool kBF16>
+struct VecTile {
+  static constexpr int kColsPerPiece = kBF16 ? 8 : 4;
+  static constexpr int kTileCols = kVecPieces * kColsPerPiece;
+  static constexpr int kColsPerStep = kBF16 ? 8 : 4;  // columns per warp step
+  static constexpr uint32_t kStageBytes = kColsPerStep * 8u * kMaxRecord;  // per warp
+  static constexpr uint32_t kSmemBytes = kVecTileBytes + kWarps * kStageBytes;
+};
+
+// Byte offset of word w (0..3) of piece p in row r of a vector tile.
+__device__ __forceinline__ uint32_t vec_word(int r, int p, int w) {
+  return static_cast<uint32_t>(r * (kVecPieces * 16) + ((p ^ ((r >> 4) & 7)) << 4) + 4 * w);
+}
+
+// Copy a run of staged records out (or in): 16-byte units when both sides allow it.
+__device__ __forceinline__ void run_copy_out(uint8_t* g, const uint8_t* s, int bytes, bool aligned,
+                                             int lane, int lanes) {
+  if (aligned) {
+    for (int i = lane; i < bytes / 16; i += lanes)
+      reinterpret_cast<uint4*>(g)[i] = reinterpret_cast<const uint4*>(s)[i];
+    for (int i = (bytes & ~15) + lane; i < bytes; i += lanes) g[i] = s[i];
+  } else {
+    for (int i = lane; i < bytes; i += lanes) g[i] = s[i];
+  }
+}
+
+__device__ __forceinline__ void run_copy_in(uint8_t* s, const uint8_t* g, int bytes, bool aligned,
+                                            int lane, int lanes) {
+  if (aligned) {
+    for (int i = lane; i < bytes / 16; i += lanes)
+      reinterpret_cast<uint4*>(s)[i] = __ldcs(reinterpret_cast<const uint4*>(g) + i);
+    for (int i = (bytes & ~15) + lane; i < bytes; i += lanes) s[i] = __ldg(g + i);
+  } else {
+    for (int i = lane; i < bytes; i += lanes) s[i] = __ldg(g + i);
+  }
+}
+
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_pack_cols_vec_kernel(const uint8_t* __restrict__ x, Geometry g, bool packed_aligned,
+                            uint8_t* __restrict__ packed) {
+  using V = VecTile<kBF16>;
+  using R = MxRule<Fmt<kFmt>::kOffset, Fmt<kFmt>::kQMax>;
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  constexpr int esize = kBF16 ? 2 : 4;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t tile = smem_u32(smem);
+  uint8_t* stage = smem + kVecTileBytes + warp * V::kStageBytes;
+  const int64_t nbl = (g.rows + 15) / 16;
+  const int64_t tiles_r = (g.rows + kVecTileRows - 1) / kVecTileRows;
+  const int64_t tiles_c = (g.cols + V::kTileCols - 1) / V::kTileCols;
+  for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int64_t tc = t % tiles_c, tr = t / tiles_c;  // across a row band first
+    const int64_t r0 = tr * kVecTileRows, c0 = tc * V::kTileCols;
+    const bool piece_ok = c0 + lane * V::kColsPerPiece < g.cols;
+    // rows in: 16 per warp, 8 loads in flight before their shared stores
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t row = r0 + warp + kWarps * (8 * h + k);
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (piece_ok && row < g.rows)
+          v[k] = __ldcs(reinterpret_cast<const uint4*>(x + (row * g.ld + c0 + lane * V::kColsPerPiece) * esize));
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        sts128(tile + vec_word(warp + kWarps * (8 * h + k), lane, 0), v[k].x, v[k].y, v[k].z, v[k].w);
+    }
+    __syncthreads();
+    const int nvalid = static_cast<int>(nbl - tr * 8 < 8 ? nbl - tr * 8 : 8);
+    const int j = lane >> 2, wsub = lane & 3;
+    for (int pg = warp; pg < kVecPieces; pg += kWarps) {
+      const int64_t colw = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + wsub * (kBF16 ? 2 : 1);
+      if (c0 + static_cast<int64_t>(pg) * V::kColsPerPiece >= g.cols) break;  // warp-uniform
+      uint32_t wd[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) wd[i] = lds32(tile + vec_word(16 * j + i, pg, wsub));
+      if (j < nvalid) {
+        uint32_t h[8], eb8, bits;
+        if (kBF16) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {  // columns colw and colw + 1
+            uint32_t w[8];
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              w[p] = __byte_perm(wd[2 * p], wd[2 * p + 1], half ? 0x7632 : 0x5410);
+            R::block_bf16(w, h, &eb8, &bits);
+            stage_record<kFmt>(smem_u32(stage) + static_cast<uint32_t>((2 * wsub + half) * 8 + j) * RB,
+                               eb8, bits, h);
+          }
+        } else {
+          R::block_f32(wd, h, &eb8, &bits);
+          stage_record<kFmt>(smem_u32(stage) + static_cast<uint32_t>(wsub * 8 + j) * RB, eb8, bits, h);
+        }
+      }
+      __syncwarp();
+      // one run of nvalid records per column; 8 lanes per run
+      const int cidx = lane >> 3;  // run handled by this lane group
+#pragma unroll
+      for (int k = 0; k < V::kColsPerStep / 4; ++k) {
+        const int ci = cidx + 4 * k;
+        const int64_t col = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + ci;
+        if (col < g.cols) {
+          const int64_t b0 = col * nbl + tr * 8;
+          run_copy_out(packed + b0 * RB, stage + ci * 8 * RB, nvalid * RB,
+                       packed_aligned && ((b0 * RB) & 15) == 0 && ((ci * 8 * RB) & 15) == 0,
+                       lane & 7, 8);
+        }
+      }
+      __syncwarp();
+      (void)colw;
+    }
+    __syncthreads();
+  }
+}
+
+// q * 2^k for the 16 elements of a staged record.
+template <int kFmt>
+__device__ __forceinline__ void decode16(uint32_t rec, float* v) {
+  uint32_t head;
+  int q[16];
+  if (kFmt == MXQ_FMT_MX9) {
+    head = lds16(rec);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t two = lds16(rec + 2u + 2u * k);
+      q[2 * k] = static_cast<int8_t>(two & 0xFFu);
+      q[2 * k + 1] = static_cast<int8_t>(two >> 8);
+    }
+  } else {
+    const uint32_t w0 = lds32(rec), w1 = lds32(rec + 4u), w2 = lds32(rec + 8u);
+    head = w0 & 0xFFFFu;
+    const uint64_t d = static_cast<uint64_t>(w0 >> 16) | (static_cast<uint64_t>(w1) << 16) |
+                       (static_cast<uint64_t>(w2) << 48);
+    const uint32_t d_hi = w2 >> 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int b = 5 * i;
+      const uint32_t c = b + 5 <= 64 ? static_cast<uint32_t>(d >> b) & 0x1Fu
+                         : b >= 64   ? (d_hi >> (b - 64)) & 0x1Fu
+                                     : (static_cast<uint32_t>(d >> b) | (d_hi << (64 - b))) & 0x1Fu;
+      q[i] = static_cast<int>(c << 27) >> 27;
+    }
+  }
+  const int eb8 = static_cast<int>(head & 0xFFu);
+  const uint32_t bits = head >> 8;
+  const float s_keep = __uint_as_float(static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset, 1)) << 23);
+  const float s_dem = __uint_as_float(static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset - 1, 1)) << 23);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    v[i] = fmul_rn_noftz(small_int_float(q[i]), (bits >> (i / 2)) & 1u ? s_dem : s_keep);
+}
+
+template <bool kBF16, int kFmt>
+__global__ void __launch_bounds__(kThreads)
+    mx_unpack_cols_vec_kernel(const uint8_t* __restrict__ packed, Geometry g, bool packed_aligned,
+                              uint8_t* __restrict__ y) {
+  using V = VecTile<kBF16>;
+  constexpr int RB = Fmt<kFmt>::kRecord;
+  constexpr int esize = kBF16 ? 2 : 4;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t tile = smem_u32(smem);
+  uint8_t* stage = smem + kVecTileBytes + warp * V::kStageBytes;
+  const int64_t nbl = (g.rows + 15) / 16;
+  const int64_t tiles_r = (g.rows + kVecTileRows - 1) / kVecTileRows;
+  const int64_t tiles_c = (g.cols + V::kTileCols - 1) / V::kTileCols;
+  for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int64_t tc = t % tiles_c, tr = t / tiles_c;
+    const int64_t r0 = tr * kVecTileRows, c0 = tc * V::kTileCols;
+    const int nvalid = static_cast<int>(nbl - tr * 8 < 8 ? nbl - tr * 8 : 8);
+    const int j = lane >> 2, wsub = lane & 3;
+    for (int pg = warp; pg < kVecPieces; pg += kWarps) {
+      if (c0 + static_cast<int64_t>(pg) * V::kColsPerPiece >= g.cols) break;  // warp-uniform
+      const int cidx = lane >> 3;
+#pragma unroll
+      for (int k = 0; k < V::kColsPerStep / 4; ++k) {
+        const int ci = cidx + 4 * k;
+        const int64_t col = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + ci;
+        if (col < g.cols) {
+          const int64_t b0 = col * nbl + tr * 8;
+          run_copy_in(stage + ci * 8 * RB, packed + b0 * RB, nvalid * RB,
+                      packed_aligned && ((b0 * RB) & 15) == 0 && ((ci * 8 * RB) & 15) == 0,
+                      lane & 7, 8);
+        }
+      }
+      __syncwarp();
+      if (j < nvalid) {
+        uint32_t wd[16];
+        if (kBF16) {
+          float a[16], b[16];
+          decode16<kFmt>(smem_u32(stage) + static_cast<uint32_t>((2 * wsub) * 8 + j) * RB, a);
+          decode16<kFmt>(smem_u32(stage) + static_cast<uint32_t>((2 * wsub + 1) * 8 + j) * RB, b);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            wd[i] = __byte_perm(__float_as_uint(a[i]), __float_as_uint(b[i]), 0x7632);
+        } else {
+          float a[16];
+          decode16<kFmt>(smem_u32(stage) + static_cast<uint32_t>(wsub * 8 + j) * RB, a);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) wd[i] = __float_as_uint(a[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sts32(tile + vec_word(16 * j + i, pg, wsub), wd[i]);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    const bool piece_ok = c0 + lane * V::kColsPerPiece < g.cols;
+#pragma unroll 8
+    for (int r = warp; r < kVecTileRows; r += kWarps) {
+      const int64_t row = r0 + r;
+      if (!piece_ok || row >= g.rows) continue;
+      const uint4 v = lds128(tile + vec_word(r, lane, 0));
+      __stcs(reinterpret_cast<uint4*>(y + (row * g.ld + c0 + lane * V::kColsPerPiece) * esize), v);
+    }
+    __syncthreads();
+  }
+}
+
+// The vector column tiles apply: 16-byte aligned base, row pitch a multiple
+// of 16 bytes, columns a whole number of 16-byte pieces.
+bool cols_vec_ok(const void* p, int dtype, int64_t cols, int64_t ld) {
+  const int64_t esize = dtype == MXQ_F32 ? 4 : 2;
+  return aligned_to(p, 16) && (ld * esize) % 16 == 0 && (cols * esize) % 16 == 0;
+}
+
+// Launch a column-tile kernel: one CTA per tile, at most a full wave.
+template <bool kBF16, bool kUnpack, bool kVec = false, typename Kernel, typename... Args>
+int launch_cols(Kernel kernel, const Geometry& g, cudaStream_t stream, Args... args) {
+  using T = ColTile<kBF16>;
+  constexpr uint32_t kSmem = kVec ? VecTile<kBF16>::kSmemBytes
+                                  : (kUnpack ? T::kUnpackSmemBytes : T::kSmemBytes);
+  constexpr int kTileRows = kVec ? kVecTileRows : kColTileRows;
+  constexpr int kTileCols = kVec ? VecTile<kBF16>::kTileCols : kColTileCols;
+  int dev = 0;
+  const int sms = sm_count_current_device(&dev);
+  if (sms <= 0) return MXQ_ECUDA;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    return MXQ_ECUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, kSmem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t tiles = ((g.rows + kTileRows - 1) / kTileRows) *
+                        ((g.cols + kTileCols - 1) / kTileCols);
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles < cap ? tiles : cap));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
+}
+
 int check_args(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, int axis, int fmt,
                const void* packed, int64_t* nb_out) {
   if (dtype != MXQ_F32 && dtype != MXQ_BF16) return MXQ_EBADDTYPE;
@@ -567,6 +1028,26 @@ extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t co
   if (flat_rows(x, rows, cols, ld, axis) && aligned_to(packed, 16))
     return launch_records_pack(x, dtype == MXQ_BF16, fmt, nb, packed, stream);
   const Geometry g{rows, cols, ld, axis};
+  if (axis == 0) {
+    const uint8_t* xc = static_cast<const uint8_t*>(x);
+    const bool pa = aligned_to(packed, 16);
+    if (cols_vec_ok(x, dtype, cols, ld)) {
+      if (dtype == MXQ_F32)
+        return fmt == MXQ_FMT_MX9
+                   ? launch_cols<false, false, true>(mx_pack_cols_vec_kernel<false, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
+                   : launch_cols<false, false, true>(mx_pack_cols_vec_kernel<false, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+      return fmt == MXQ_FMT_MX9
+                 ? launch_cols<true, false, true>(mx_pack_cols_vec_kernel<true, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
+                 : launch_cols<true, false, true>(mx_pack_cols_vec_kernel<true, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+    }
+    if (dtype == MXQ_F32)
+      return fmt == MXQ_FMT_MX9
+                 ? launch_cols<false, false>(mx_pack_cols_kernel<false, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
+                 : launch_cols<false, false>(mx_pack_cols_kernel<false, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+    return fmt == MXQ_FMT_MX9
+               ? launch_cols<true, false>(mx_pack_cols_kernel<true, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
+               : launch_cols<true, false>(mx_pack_cols_kernel<true, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+  }
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
   const bool vec_rows = aligned_to(x, 16) && (ld * esize) % 16 == 0;
   const bool pal = aligned_to(packed, 16);
@@ -596,6 +1077,25 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
                : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb);
   }
   const Geometry g{rows, cols, ld, axis};
+  if (axis == 0) {
+    const bool pa = aligned_to(packed, 16);
+    if (cols_vec_ok(y, dtype, cols, ld)) {
+      if (dtype == MXQ_F32)
+        return fmt == MXQ_FMT_MX9
+                   ? launch_cols<false, true, true>(mx_unpack_cols_vec_kernel<false, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
+                   : launch_cols<false, true, true>(mx_unpack_cols_vec_kernel<false, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+      return fmt == MXQ_FMT_MX9
+                 ? launch_cols<true, true, true>(mx_unpack_cols_vec_kernel<true, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
+                 : launch_cols<true, true, true>(mx_unpack_cols_vec_kernel<true, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+    }
+    if (dtype == MXQ_F32)
+      return fmt == MXQ_FMT_MX9
+                 ? launch_cols<false, true>(mx_unpack_cols_kernel<false, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
+                 : launch_cols<false, true>(mx_unpack_cols_kernel<false, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+    return fmt == MXQ_FMT_MX9
+               ? launch_cols<true, true>(mx_unpack_cols_kernel<true, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
+               : launch_cols<true, true>(mx_unpack_cols_kernel<true, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+  }
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
   const bool vec_rows = aligned_to(y, 16) && (ld * esize) % 16 == 0;
   const bool pal = aligned_to(packed, 16);

@@ -113,7 +113,7 @@ def test_packed_offsets_below_16_bytes(fmt, dt, x_off, p_off):
         x = W.f32_to_bf16_bits(x)
     rb, nb = mxq.RECORD_BYTES[fmt], rows * cols // 16
     want = oracle.mx_pack(x, fmt, axis=1)
-    flat = np.concatenate([np.zeros(1, x.dtype), x.reshape(-1)])
+    flat = np.concatenate([np.zeros(x_off, x.dtype), x.reshape(-1)])  # data from element x_off
     xd = _dev(flat)[x_off:x_off + rows * cols].view(rows, cols)
     poff = (2 if fmt == mxq.FMT_MX9 else 4) * p_off
     big = torch.zeros(nb * rb + 16, dtype=torch.uint8, device="cuda")
