@@ -130,12 +130,15 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
       : "memory");
 }
 
-// kSplit: q [nb, 16] int8, max_exp [nb], prime [nb].  kRecMx9 / kRecMx6: out
-// is the packed tensor of nb records (16-byte aligned); q_or_rec points to it.
+// x: nb blocks in rows of nbl blocks, rows pitch bytes apart (16-byte aligned
+// starts).  kSplit: q [nb, 16] int8, max_exp [nb], prime [nb].  kRecMx9 /
+// kRecMx6: out is the packed tensor of nb records (16-byte aligned); q_or_rec
+// points to it.
 template <bool kBF16, int kOut>
 __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK_CTAS_PER_SM)
-    mx9_pack_kernel(const uint8_t* __restrict__ x, int64_t nb, uint8_t* __restrict__ q_or_rec,
-                    uint8_t* __restrict__ max_exp, uint8_t* __restrict__ prime) {
+    mx9_pack_kernel(const uint8_t* __restrict__ x, int64_t nb, int64_t nbl, int64_t pitch,
+                    uint8_t* __restrict__ q_or_rec, uint8_t* __restrict__ max_exp,
+                    uint8_t* __restrict__ prime) {
   using S = PackShape<kBF16, kOut>;
   using R = MxRule<kOut == kRecMx6 ? 3 : 6, kOut == kRecMx6 ? 15 : 127>;
   extern __shared__ uint8_t smem_raw[];
@@ -175,8 +178,19 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
       const int64_t nblk = nb - b0 < S::kBlocksPerStage ? nb - b0 : S::kBlocksPerStage;
       const uint32_t bytes = static_cast<uint32_t>(nblk) * S::kBlockBytes;
       mbar_arrive_expect_tx(full(s), bytes);
-      bulk_load_1d(base + static_cast<uint32_t>(s) * S::kStageBytes, x + b0 * S::kBlockBytes,
-                   bytes, full(s));
+      const uint32_t dst = base + static_cast<uint32_t>(s) * S::kStageBytes;
+      if (pitch == nbl * static_cast<int64_t>(S::kBlockBytes)) {  // rows follow each other
+        bulk_load_1d(dst, x + b0 * S::kBlockBytes, bytes, full(s));
+      } else {  // one copy per row piece of the stage's blocks
+        int64_t row = b0 / nbl, j = b0 - row * nbl;
+        for (int64_t b = b0; b < b0 + nblk; ++row, j = 0) {
+          const int64_t n = b0 + nblk - b < nbl - j ? b0 + nblk - b : nbl - j;
+          bulk_load_1d(dst + static_cast<uint32_t>(b - b0) * S::kBlockBytes,
+                       x + row * pitch + j * S::kBlockBytes,
+                       static_cast<uint32_t>(n) * S::kBlockBytes, full(s));
+          b += n;
+        }
+      }
       issued = i + 1;
     }
     // drain (a no-op after a normal run: consumers waited for every stage)
@@ -397,8 +411,8 @@ int check_dims(int dtype, int64_t rows, int64_t cols) {
 }
 
 template <bool kBF16, int kOut>
-cudaError_t launch_pack(const void* x, int64_t nb, uint8_t* q_or_rec, uint8_t* max_exp,
-                        uint8_t* prime, int sms, int dev, cudaStream_t stream) {
+cudaError_t launch_pack(const void* x, int64_t nb, int64_t nbl, int64_t pitch, uint8_t* q_or_rec,
+                        uint8_t* max_exp, uint8_t* prime, int sms, int dev, cudaStream_t stream) {
   using S = PackShape<kBF16, kOut>;
   static bool attr_done[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -416,7 +430,7 @@ cudaError_t launch_pack(const void* x, int64_t nb, uint8_t* q_or_rec, uint8_t* m
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, mx9_pack_kernel<kBF16, kOut>, static_cast<const uint8_t*>(x),
-                            nb, q_or_rec, max_exp, prime);
+                            nb, nbl, pitch, q_or_rec, max_exp, prime);
 }
 
 }  // namespace
@@ -435,18 +449,18 @@ int mx9_status_read(unsigned int* out, bool clear) {
 // The packed-record form of the pack kernel for a contiguous tensor blocked
 // along its rows (x and packed 16-byte aligned, nb whole blocks); the caller
 // has checked the arguments.
-int launch_records_pack(const void* x, bool bf16, int fmt, int64_t nb, uint8_t* packed,
-                        cudaStream_t stream) {
+int launch_records_pack(const void* x, bool bf16, int fmt, int64_t nb, int64_t nbl, int64_t pitch,
+                        uint8_t* packed, cudaStream_t stream) {
   int dev = 0;
   const int sms = sm_count_current_device(&dev);
   if (sms <= 0) return MXQ_ECUDA;
   cudaError_t e;
   if (fmt == MXQ_FMT_MX9)
-    e = bf16 ? launch_pack<true, kRecMx9>(x, nb, packed, nullptr, nullptr, sms, dev, stream)
-             : launch_pack<false, kRecMx9>(x, nb, packed, nullptr, nullptr, sms, dev, stream);
+    e = bf16 ? launch_pack<true, kRecMx9>(x, nb, nbl, pitch, packed, nullptr, nullptr, sms, dev, stream)
+             : launch_pack<false, kRecMx9>(x, nb, nbl, pitch, packed, nullptr, nullptr, sms, dev, stream);
   else
-    e = bf16 ? launch_pack<true, kRecMx6>(x, nb, packed, nullptr, nullptr, sms, dev, stream)
-             : launch_pack<false, kRecMx6>(x, nb, packed, nullptr, nullptr, sms, dev, stream);
+    e = bf16 ? launch_pack<true, kRecMx6>(x, nb, nbl, pitch, packed, nullptr, nullptr, sms, dev, stream)
+             : launch_pack<false, kRecMx6>(x, nb, nbl, pitch, packed, nullptr, nullptr, sms, dev, stream);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 }  // namespace mxq
@@ -471,9 +485,11 @@ extern "C" int mx9_pack(const void* x, int dtype, int64_t rows, int64_t cols, in
   const int sms = sm_count_current_device(&dev);
   if (sms <= 0) return MXQ_ECUDA;
   uint8_t* qb = reinterpret_cast<uint8_t*>(q);
+  const int64_t nb = n / 16;  // one flat run of blocks
   const cudaError_t e =
-      dtype == MXQ_F32 ? launch_pack<false, kSplit>(x, n / 16, qb, max_exp, prime, sms, dev, stream)
-                       : launch_pack<true, kSplit>(x, n / 16, qb, max_exp, prime, sms, dev, stream);
+      dtype == MXQ_F32
+          ? launch_pack<false, kSplit>(x, nb, nb, nb * 64, qb, max_exp, prime, sms, dev, stream)
+          : launch_pack<true, kSplit>(x, nb, nb, nb * 32, qb, max_exp, prime, sms, dev, stream);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 

@@ -12,11 +12,12 @@
 // 5-bit two's-complement codes, element i at bits 5i..5i+4 of the 10 data
 // bytes read as one little-endian number.
 //
-// A contiguous tensor blocked along its rows (the common case) is a flat run
-// of whole blocks: packing goes through the TMA-fed pack kernel of mx9.cu in
-// its record form, and unpacking through mx_unpack_records_kernel below, where
-// a warp copies 32 records into shared memory with 16-byte loads and each lane
-// then writes 16 output bytes.  Every other geometry (blocks along columns,
+// A tensor blocked along its rows with whole blocks per row and 16-byte
+// aligned rows (the common case) is a run of whole blocks, row by row: packing
+// goes through the TMA-fed pack kernel of mx9.cu in its record form, and
+// unpacking through mx_unpack_records_kernel below, where a warp copies runs
+// of records into shared memory with 16-byte loads and each lane then writes
+// 16 output bytes.  Every other geometry (blocks along columns,
 // strided rows, partial blocks) takes the generic kernels: one thread owns one
 // block; along axis 1 (a row) a warp's 32 blocks are consecutive records,
 // staged in shared memory and moved with 16-byte coalesced copies; along axis
@@ -418,15 +419,17 @@ __device__ __forceinline__ float small_int_float(int32_t q) {
 constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight per warp
 
 // Unpack of a contiguous tensor blocked along its rows: nb records, the
-// output is nb * 16 elements.  Each warp takes kRecRuns consecutive runs of 32
+// output is nb * 16 elements in rows of nbl blocks, ld elements apart (ld ==
+// 16 nbl: one flat run; otherwise nbl >= 32 kRecRuns, so that the records a
+// warp takes at once span at most two rows).  Each warp takes kRecRuns consecutive runs of 32
 // records at a time: copies them into shared memory with 16-byte loads (all
 // loads issued before the first shared store), then each lane rebuilds 16
 // output bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp
 // cover 512 contiguous bytes.  packed and y are 16-byte aligned.
 template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
-    mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb,
-                             uint8_t* __restrict__ y) {
+    mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
+                             int64_t ld, uint8_t* __restrict__ y) {
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int kElems = kBF16 ? 8 : 4;  // elements per 16 output bytes
   constexpr int kParts = 16 / kElems;    // output units per block
@@ -437,9 +440,11 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t st = smem_u32(stage[warp]);
   const int64_t ngroups = (nb + kGroup - 1) / kGroup;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kWarps;
+  const bool flat = ld == nbl * 16;  // else rows of nbl >= kGroup blocks, ld elements apart
   for (int64_t grp = static_cast<int64_t>(blockIdx.x) * kWarps + warp; grp < ngroups;
        grp += wstride) {
     const int64_t r0 = grp * kGroup;
+    const int64_t row0 = flat ? 0 : r0 / nbl, j0 = flat ? 0 : r0 - row0 * nbl;
     const int nvalid = static_cast<int>(nb - r0 < kGroup ? nb - r0 : kGroup);
     // copy in: 16-byte units, then 2-byte pieces
     const uint8_t* src = packed + r0 * RB;
@@ -501,15 +506,26 @@ __global__ void __launch_bounds__(kThreads)
                                           : static_cast<int>(code[k] << 27) >> 27;
         val[k] = fmul_rn_noftz(small_int_float(q), sc);
       }
-      const int64_t unit = (r0 + r) * kParts + part;  // 16-byte output unit
+      int64_t elem;  // first output element of this 16-byte unit
+      if (flat) {
+        elem = (r0 + r) * 16 + part * kElems;
+      } else {  // a group spans at most two rows
+        int64_t jr = j0 + r, rr = row0;
+        if (jr >= nbl) {
+          jr -= nbl;
+          ++rr;
+        }
+        elem = rr * ld + jr * 16 + part * kElems;
+      }
+      uint8_t* dst = y + elem * (kBF16 ? 2 : 4);
       if (kBF16) {
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           o[k] = __byte_perm(__float_as_uint(val[2 * k]), __float_as_uint(val[2 * k + 1]), 0x7632);
-        __stcs(reinterpret_cast<uint4*>(y) + unit, make_uint4(o[0], o[1], o[2], o[3]));
+        __stcs(reinterpret_cast<uint4*>(dst), make_uint4(o[0], o[1], o[2], o[3]));
       } else {
-        __stcs(reinterpret_cast<float4*>(y) + unit, make_float4(val[0], val[1], val[2], val[3]));
+        __stcs(reinterpret_cast<float4*>(dst), make_float4(val[0], val[1], val[2], val[3]));
       }
     }
     __syncwarp();
@@ -998,10 +1014,14 @@ int check_args(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
   return MXQ_OK;
 }
 
-// A tensor blocked along its rows whose rows follow each other with no gap and
-// hold whole blocks: a flat run of 16-element blocks.
-bool flat_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, int axis) {
-  return axis == 1 && cols % 16 == 0 && (ld == cols || rows == 1) && aligned_to(x, 16);
+// A tensor blocked along its rows that the record kernels take: whole blocks
+// per row, 16-byte aligned base and row pitch, and rows either following each
+// other or holding at least min_nbl blocks (long enough for per-row handling).
+bool rows_ok(const void* p, int dtype, int64_t rows, int64_t cols, int64_t ld, int axis,
+             int64_t min_nbl) {
+  const int64_t esize = dtype == MXQ_F32 ? 4 : 2;
+  if (axis != 1 || cols % 16 != 0 || !aligned_to(p, 16) || (ld * esize) % 16 != 0) return false;
+  return ld == cols || rows == 1 || cols / 16 >= min_nbl;
 }
 
 // One thread per work item (capped at a full wave of 8 blocks per SM).
@@ -1025,8 +1045,11 @@ extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t co
   int64_t nb = 0;
   const int rc = check_args(x, dtype, rows, cols, ld, axis, fmt, packed, &nb);
   if (rc != MXQ_OK || nb == 0) return rc;
-  if (flat_rows(x, rows, cols, ld, axis) && aligned_to(packed, 16))
-    return launch_records_pack(x, dtype == MXQ_BF16, fmt, nb, packed, stream);
+  if (rows_ok(x, dtype, rows, cols, ld, axis, 32) && aligned_to(packed, 16)) {
+    const int64_t esize = dtype == MXQ_F32 ? 4 : 2;
+    return launch_records_pack(x, dtype == MXQ_BF16, fmt, nb, cols / 16,
+                               (rows == 1 ? cols : ld) * esize, packed, stream);
+  }
   const Geometry g{rows, cols, ld, axis};
   if (axis == 0) {
     const uint8_t* xc = static_cast<const uint8_t*>(x);
@@ -1067,14 +1090,15 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   const int rc = check_args(y, dtype, rows, cols, ld, axis, fmt, packed, &nb);
   if (rc != MXQ_OK || nb == 0) return rc;
   uint8_t* yb = static_cast<uint8_t*>(y);
-  if (flat_rows(y, rows, cols, ld, axis) && aligned_to(packed, 16)) {
+  if (rows_ok(y, dtype, rows, cols, ld, axis, 32 * kRecRuns) && aligned_to(packed, 16)) {
+    const int64_t nbl = cols / 16, pitch = rows == 1 ? cols : ld;
     if (dtype == MXQ_F32)
       return fmt == MXQ_FMT_MX9
-                 ? launch(mx_unpack_records_kernel<false, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb)
-                 : launch(mx_unpack_records_kernel<false, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb);
+                 ? launch(mx_unpack_records_kernel<false, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb)
+                 : launch(mx_unpack_records_kernel<false, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb);
     return fmt == MXQ_FMT_MX9
-               ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb)
-               : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, yb);
+               ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb)
+               : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb);
   }
   const Geometry g{rows, cols, ld, axis};
   if (axis == 0) {

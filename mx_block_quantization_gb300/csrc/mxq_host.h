@@ -52,9 +52,10 @@ inline int sm_count_current_device(int* out_device) {
 }
 
 // Launch the packed-record form of the TMA-fed pack kernel (mx9.cu) over nb
-// whole 16-element blocks of a contiguous tensor blocked along its rows; x and
-// packed 16-byte aligned, arguments already checked.  Returns an MXQ_* code.
-int launch_records_pack(const void* x, bool bf16, int fmt, int64_t nb, uint8_t* packed,
-                        cudaStream_t stream);
+// whole 16-element blocks of a tensor blocked along its rows: rows of nbl
+// blocks, pitch bytes apart; x, packed and pitch 16-byte aligned, arguments
+// already checked.  Returns an MXQ_* code.
+int launch_records_pack(const void* x, bool bf16, int fmt, int64_t nb, int64_t nbl, int64_t pitch,
+                        uint8_t* packed, cudaStream_t stream);
 
 }  // namespace mxq

@@ -55,7 +55,8 @@ def _check(x_full: np.ndarray, cols: int, fmt: int, axis: int, tag: str):
 @pytest.mark.parametrize("rows,cols,ld", [(64, 256, 256), (20, 37, 37), (48, 80, 112),
                                           (33, 16, 24), (1, 15, 15), (257, 129, 136),
                                           (3, 16, 16), (7, 48, 48), (1000, 160, 160),
-                                          (1, 4096, 4096), (129, 2048, 2048)])
+                                          (1, 4096, 4096), (129, 2048, 2048),
+                                          (40, 512, 528), (33, 2048, 2064), (5, 4096, 4224)])
 def test_packed_shapes(fmt, dt, axis, rows, cols, ld):
     x = np.zeros((rows, ld), np.float32)
     x[:, :cols] = W.mx9_outliers(rows, cols, seed=rows * cols + axis, zero_blocks=0, tiny_blocks=0)
