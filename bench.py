@@ -541,6 +541,28 @@ def run_sweep(mxq, torch, dev, rank):
             speedups.append(speedup)
             print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
+    # the packed tensor in its other geometries: blocks along columns, and
+    # blocked rows at a pitch of cols + 64 (the input a strided view)
+    M, N = 16384, 8192
+    line = {"sweep_packed_geometries": [M, N], "peak_gbs": peak, "peak_kind": kind}
+    for dt, tdt, esz in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        wide = torch.from_numpy(W.normal_f32((M, N + 64), seed=0)).to(dev).to(tdt)
+        ywide = torch.empty_like(wide)
+        for layout, xin, yout, axis in (("axis0", wide[:, :N].contiguous(), None, 0),
+                                        ("pitched_rows", wide[:, :N], ywide[:, :N], 1)):
+            yy = torch.empty_like(xin) if yout is None else yout
+            for fmt, name in ((mxq.FMT_MX9, "mx9"), (mxq.FMT_MX6, "mx6")):
+                rec = mxq.mx_pack_packed(xin, fmt, axis)
+                pbytes = (esz + mxq.RECORD_BYTES[fmt] / 16) * M * N
+                for op, launch in (("pack", lambda s: mxq.mx_pack_packed(xin, fmt, axis, out=rec, stream=s)),
+                                   ("unpack", lambda s: mxq.mx_unpack_packed(rec, fmt, yy, axis, stream=s))):
+                    gbs = pbytes / (graph_time(torch, dev, launch) / 1e6) / 1e9
+                    line[f"{name}_{layout}_{op}_{dt}"] = {"gbs": gbs, "frac_of_measured": gbs / peak}
+                del rec
+        del wide, ywide
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    torch.cuda.empty_cache()
     if rank == 0:
         geo = float(np.exp(np.mean(np.log(speedups))))
         print(json.dumps({"sweep_summary": "fused dual-axis cast vs three-pass composition, "

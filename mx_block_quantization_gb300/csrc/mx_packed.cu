@@ -965,8 +965,8 @@ bool cols_vec_ok(const void* p, int dtype, int64_t cols, int64_t ld) {
 }
 
 // Launch a column-tile kernel: one CTA per tile, at most a full wave.
-template <bool kBF16, bool kUnpack, bool kVec = false, typename Kernel, typename... Args>
-int launch_cols(Kernel kernel, const Geometry& g, cudaStream_t stream, Args... args) {
+template <bool kBF16, bool kUnpack, bool kVec, auto kernel, typename... Args>
+int launch_cols(const Geometry& g, cudaStream_t stream, Args... args) {
   using T = ColTile<kBF16>;
   constexpr uint32_t kSmem = kVec ? VecTile<kBF16>::kSmemBytes
                                   : (kUnpack ? T::kUnpackSmemBytes : T::kSmemBytes);
@@ -975,13 +975,22 @@ int launch_cols(Kernel kernel, const Geometry& g, cudaStream_t stream, Args... a
   int dev = 0;
   const int sms = sm_count_current_device(&dev);
   if (sms <= 0) return MXQ_ECUDA;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
-    return MXQ_ECUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, kSmem) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  if (dev < 0 || dev >= 64) return MXQ_ECUDA;
+  // once per kernel and device, so that later calls (inside a CUDA-graph
+  // capture, for instance) only enqueue the launch; a benign race sets the
+  // same values twice
+  static int per_sm_cache[64] = {};
+  int per_sm = per_sm_cache[dev];
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
+      return MXQ_ECUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, kSmem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    per_sm_cache[dev] = per_sm;
+  }
   const int64_t tiles = ((g.rows + kTileRows - 1) / kTileRows) *
                         ((g.cols + kTileCols - 1) / kTileCols);
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
@@ -1057,19 +1066,19 @@ extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t co
     if (cols_vec_ok(x, dtype, cols, ld)) {
       if (dtype == MXQ_F32)
         return fmt == MXQ_FMT_MX9
-                   ? launch_cols<false, false, true>(mx_pack_cols_vec_kernel<false, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
-                   : launch_cols<false, false, true>(mx_pack_cols_vec_kernel<false, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+                   ? launch_cols<false, false, true, mx_pack_cols_vec_kernel<false, MXQ_FMT_MX9>>(g, stream, xc, g, pa, packed)
+                   : launch_cols<false, false, true, mx_pack_cols_vec_kernel<false, MXQ_FMT_MX6>>(g, stream, xc, g, pa, packed);
       return fmt == MXQ_FMT_MX9
-                 ? launch_cols<true, false, true>(mx_pack_cols_vec_kernel<true, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
-                 : launch_cols<true, false, true>(mx_pack_cols_vec_kernel<true, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+                 ? launch_cols<true, false, true, mx_pack_cols_vec_kernel<true, MXQ_FMT_MX9>>(g, stream, xc, g, pa, packed)
+                 : launch_cols<true, false, true, mx_pack_cols_vec_kernel<true, MXQ_FMT_MX6>>(g, stream, xc, g, pa, packed);
     }
     if (dtype == MXQ_F32)
       return fmt == MXQ_FMT_MX9
-                 ? launch_cols<false, false>(mx_pack_cols_kernel<false, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
-                 : launch_cols<false, false>(mx_pack_cols_kernel<false, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+                 ? launch_cols<false, false, false, mx_pack_cols_kernel<false, MXQ_FMT_MX9>>(g, stream, xc, g, pa, packed)
+                 : launch_cols<false, false, false, mx_pack_cols_kernel<false, MXQ_FMT_MX6>>(g, stream, xc, g, pa, packed);
     return fmt == MXQ_FMT_MX9
-               ? launch_cols<true, false>(mx_pack_cols_kernel<true, MXQ_FMT_MX9>, g, stream, xc, g, pa, packed)
-               : launch_cols<true, false>(mx_pack_cols_kernel<true, MXQ_FMT_MX6>, g, stream, xc, g, pa, packed);
+               ? launch_cols<true, false, false, mx_pack_cols_kernel<true, MXQ_FMT_MX9>>(g, stream, xc, g, pa, packed)
+               : launch_cols<true, false, false, mx_pack_cols_kernel<true, MXQ_FMT_MX6>>(g, stream, xc, g, pa, packed);
   }
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
   const bool vec_rows = aligned_to(x, 16) && (ld * esize) % 16 == 0;
@@ -1106,19 +1115,19 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
     if (cols_vec_ok(y, dtype, cols, ld)) {
       if (dtype == MXQ_F32)
         return fmt == MXQ_FMT_MX9
-                   ? launch_cols<false, true, true>(mx_unpack_cols_vec_kernel<false, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
-                   : launch_cols<false, true, true>(mx_unpack_cols_vec_kernel<false, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+                   ? launch_cols<false, true, true, mx_unpack_cols_vec_kernel<false, MXQ_FMT_MX9>>(g, stream, packed, g, pa, yb)
+                   : launch_cols<false, true, true, mx_unpack_cols_vec_kernel<false, MXQ_FMT_MX6>>(g, stream, packed, g, pa, yb);
       return fmt == MXQ_FMT_MX9
-                 ? launch_cols<true, true, true>(mx_unpack_cols_vec_kernel<true, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
-                 : launch_cols<true, true, true>(mx_unpack_cols_vec_kernel<true, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+                 ? launch_cols<true, true, true, mx_unpack_cols_vec_kernel<true, MXQ_FMT_MX9>>(g, stream, packed, g, pa, yb)
+                 : launch_cols<true, true, true, mx_unpack_cols_vec_kernel<true, MXQ_FMT_MX6>>(g, stream, packed, g, pa, yb);
     }
     if (dtype == MXQ_F32)
       return fmt == MXQ_FMT_MX9
-                 ? launch_cols<false, true>(mx_unpack_cols_kernel<false, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
-                 : launch_cols<false, true>(mx_unpack_cols_kernel<false, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+                 ? launch_cols<false, true, false, mx_unpack_cols_kernel<false, MXQ_FMT_MX9>>(g, stream, packed, g, pa, yb)
+                 : launch_cols<false, true, false, mx_unpack_cols_kernel<false, MXQ_FMT_MX6>>(g, stream, packed, g, pa, yb);
     return fmt == MXQ_FMT_MX9
-               ? launch_cols<true, true>(mx_unpack_cols_kernel<true, MXQ_FMT_MX9>, g, stream, packed, g, pa, yb)
-               : launch_cols<true, true>(mx_unpack_cols_kernel<true, MXQ_FMT_MX6>, g, stream, packed, g, pa, yb);
+               ? launch_cols<true, true, false, mx_unpack_cols_kernel<true, MXQ_FMT_MX9>>(g, stream, packed, g, pa, yb)
+               : launch_cols<true, true, false, mx_unpack_cols_kernel<true, MXQ_FMT_MX6>>(g, stream, packed, g, pa, yb);
   }
   const uintptr_t esize = dtype == MXQ_F32 ? 4 : 2;
   const bool vec_rows = aligned_to(y, 16) && (ld * esize) % 16 == 0;

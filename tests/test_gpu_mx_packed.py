@@ -131,3 +131,29 @@ def test_packed_offsets_below_16_bytes(fmt, dt, x_off, p_off):
     torch.cuda.synchronize()
     got = yd.cpu().view(torch.int16 if is_bf16 else torch.int32).numpy()
     assert_bytes_equal(got.view(np.uint8), ref.view(np.uint8), f"fmt{fmt} {dt} unpack offsets")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("axis,pitch", [(1, 0), (1, 64), (0, 0), (0, 8)])
+def test_packed_calls_replay_in_a_cuda_graph(fmt, axis, pitch):
+    """After one eager call (which sets up each kernel), pack and unpack record
+    into a CUDA graph and its replay gives the eager bytes."""
+    rows, cols = 256, 1024
+    wide = _dev(W.normal_f32((rows, cols + pitch), seed=31))
+    x = wide[:, :cols]
+    rec = mxq.mx_pack_packed(x, fmt, axis)
+    y = torch.empty_like(wide)[:, :cols]
+    mxq.mx_unpack_packed(rec, fmt, y, axis)
+    torch.cuda.synchronize()
+    rec_eager, y_eager = rec.clone(), y.clone()
+    rec.zero_()
+    y.zero_()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mxq.mx_pack_packed(x, fmt, axis, out=rec, stream=s)
+        mxq.mx_unpack_packed(rec, fmt, y, axis, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(rec, rec_eager)
+    assert torch.equal(y.contiguous().view(torch.int32), y_eager.contiguous().view(torch.int32))
