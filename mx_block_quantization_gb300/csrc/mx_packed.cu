@@ -720,6 +720,26 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// 16-byte asynchronous copy global -> shared (cache in L2 only); src_bytes 0
+// writes zeros without reading.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Vector form of the column tiles, for tensors whose rows can be moved in
 // 16-byte pieces (16-byte aligned base, row pitch a multiple of 16 bytes,
 // columns a multiple of a piece).  A tile is 128 rows (8 blocks) x 32 pieces
@@ -741,6 +761,9 @@ struct VecTile {
   static constexpr int kColsPerStep = kBF16 ? 8 : 4;  // columns per warp step
   static constexpr uint32_t kStageBytes = kColsPerStep * 8u * kMaxRecord;  // per warp
   static constexpr uint32_t kSmemBytes = kVecTileBytes + kWarps * kStageBytes;
+  // unpack: two staging slots per warp (the next step's records arrive while
+  // the current step decodes)
+  static constexpr uint32_t kUnpackSmemBytes = kVecTileBytes + kWarps * 2u * kStageBytes;
 };
 
 // Byte offset of word w (0..3) of piece p in row r of a vector tile.
@@ -790,21 +813,17 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t tc = t % tiles_c, tr = t / tiles_c;  // across a row band first
     const int64_t r0 = tr * kVecTileRows, c0 = tc * V::kTileCols;
     const bool piece_ok = c0 + lane * V::kColsPerPiece < g.cols;
-    // rows in: 16 per warp, 8 loads in flight before their shared stores
+    // rows in: 16 per warp, each lane's pieces copied asynchronously straight
+    // to their swizzled places (zero-filled outside the tensor)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint4 v[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int64_t row = r0 + warp + kWarps * (8 * h + k);
-        v[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (piece_ok && row < g.rows)
-          v[k] = __ldcs(reinterpret_cast<const uint4*>(x + (row * g.ld + c0 + lane * V::kColsPerPiece) * esize));
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        sts128(tile + vec_word(warp + kWarps * (8 * h + k), lane, 0), v[k].x, v[k].y, v[k].z, v[k].w);
+    for (int k = 0; k < kVecTileRows / kWarps; ++k) {
+      const int r = warp + kWarps * k;
+      const int64_t row = r0 + r;
+      const bool in = piece_ok && row < g.rows;
+      const uint8_t* src = in ? x + (row * g.ld + c0 + lane * V::kColsPerPiece) * esize : x;
+      cp_async_16(tile + vec_word(r, lane, 0), src, in ? 16u : 0u);
     }
+    cp_async_wait_all();
     __syncthreads();
     const int nvalid = static_cast<int>(nbl - tr * 8 < 8 ? nbl - tr * 8 : 8);
     const int j = lane >> 2, wsub = lane & 3;
@@ -897,52 +916,80 @@ __global__ void __launch_bounds__(kThreads)
   using V = VecTile<kBF16>;
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int esize = kBF16 ? 2 : 4;
+  constexpr int kRunBytes = 8 * RB;  // one column's 8 records in a tile
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t tile = smem_u32(smem);
-  uint8_t* stage = smem + kVecTileBytes + warp * V::kStageBytes;
+  uint8_t* stage = smem + kVecTileBytes + warp * 2 * V::kStageBytes;
   const int64_t nbl = (g.rows + 15) / 16;
   const int64_t tiles_r = (g.rows + kVecTileRows - 1) / kVecTileRows;
   const int64_t tiles_c = (g.cols + V::kTileCols - 1) / V::kTileCols;
+  // records arrive by 16-byte asynchronous copies when every run starts on a
+  // 16-byte boundary, else by plain loads
+  const bool async_in = packed_aligned && ((nbl * RB) & 15) == 0;
+  const int cidx = lane >> 3;  // run of this lane group (8 lanes per run)
   for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
     const int64_t tc = t % tiles_c, tr = t / tiles_c;
     const int64_t r0 = tr * kVecTileRows, c0 = tc * V::kTileCols;
     const int nvalid = static_cast<int>(nbl - tr * 8 < 8 ? nbl - tr * 8 : 8);
-    const int j = lane >> 2, wsub = lane & 3;
-    for (int pg = warp; pg < kVecPieces; pg += kWarps) {
-      if (c0 + static_cast<int64_t>(pg) * V::kColsPerPiece >= g.cols) break;  // warp-uniform
-      const int cidx = lane >> 3;
+    const int bytes = nvalid * RB;
+    int nsteps = 0;  // piece groups of this warp inside the tensor
+    for (int pg = warp; pg < kVecPieces && c0 + static_cast<int64_t>(pg) * V::kColsPerPiece < g.cols;
+         pg += kWarps)
+      ++nsteps;
+    // fetch the runs of step k into slot k & 1
+    auto fetch = [&](int k) {
+      const int pg = warp + kWarps * k;
+      uint8_t* slot = stage + (k & 1) * V::kStageBytes;
 #pragma unroll
-      for (int k = 0; k < V::kColsPerStep / 4; ++k) {
-        const int ci = cidx + 4 * k;
+      for (int m = 0; m < V::kColsPerStep / 4; ++m) {
+        const int ci = cidx + 4 * m;
         const int64_t col = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + ci;
-        if (col < g.cols) {
-          const int64_t b0 = col * nbl + tr * 8;
-          run_copy_in(stage + ci * 8 * RB, packed + b0 * RB, nvalid * RB,
-                      packed_aligned && ((b0 * RB) & 15) == 0 && ((ci * 8 * RB) & 15) == 0,
-                      lane & 7, 8);
+        const uint8_t* src = packed + (col * nbl + tr * 8) * RB;
+        uint8_t* dst = slot + ci * kRunBytes;
+        if (async_in) {
+          for (int u = lane & 7; u < (kRunBytes + 15) / 16; u += 8) {
+            const int left = bytes - 16 * u;
+            cp_async_16(smem_u32(dst) + 16u * u, left > 0 ? src + 16 * u : packed,
+                        left >= 16 ? 16u : (left > 0 ? static_cast<uint32_t>(left) : 0u));
+          }
+        } else {
+          run_copy_in(dst, src, bytes, false, lane & 7, 8);
         }
       }
+      cp_async_commit();
+    };
+    if (nsteps > 0) fetch(0);
+    for (int k = 0; k < nsteps; ++k) {
+      if (k + 1 < nsteps) {
+        fetch(k + 1);
+        cp_async_wait_group<1>();
+      } else {
+        cp_async_wait_group<0>();
+      }
       __syncwarp();
+      const int pg = warp + kWarps * k;
+      const uint8_t* slot = stage + (k & 1) * V::kStageBytes;
+      const int j = lane >> 2, wsub = lane & 3;
       if (j < nvalid) {
         uint32_t wd[16];
         if (kBF16) {
           float a[16], b[16];
-          decode16<kFmt>(smem_u32(stage) + static_cast<uint32_t>((2 * wsub) * 8 + j) * RB, a);
-          decode16<kFmt>(smem_u32(stage) + static_cast<uint32_t>((2 * wsub + 1) * 8 + j) * RB, b);
+          decode16<kFmt>(smem_u32(slot) + static_cast<uint32_t>((2 * wsub) * 8 + j) * RB, a);
+          decode16<kFmt>(smem_u32(slot) + static_cast<uint32_t>((2 * wsub + 1) * 8 + j) * RB, b);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             wd[i] = __byte_perm(__float_as_uint(a[i]), __float_as_uint(b[i]), 0x7632);
         } else {
           float a[16];
-          decode16<kFmt>(smem_u32(stage) + static_cast<uint32_t>(wsub * 8 + j) * RB, a);
+          decode16<kFmt>(smem_u32(slot) + static_cast<uint32_t>(wsub * 8 + j) * RB, a);
 #pragma unroll
           for (int i = 0; i < 16; ++i) wd[i] = __float_as_uint(a[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) sts32(tile + vec_word(16 * j + i, pg, wsub), wd[i]);
       }
-      __syncwarp();
+      __syncwarp();  // slot k & 1 is refilled at step k + 2
     }
     __syncthreads();
     const bool piece_ok = c0 + lane * V::kColsPerPiece < g.cols;
@@ -968,8 +1015,9 @@ bool cols_vec_ok(const void* p, int dtype, int64_t cols, int64_t ld) {
 template <bool kBF16, bool kUnpack, bool kVec, auto kernel, typename... Args>
 int launch_cols(const Geometry& g, cudaStream_t stream, Args... args) {
   using T = ColTile<kBF16>;
-  constexpr uint32_t kSmem = kVec ? VecTile<kBF16>::kSmemBytes
-                                  : (kUnpack ? T::kUnpackSmemBytes : T::kSmemBytes);
+  constexpr uint32_t kSmem =
+      kVec ? (kUnpack ? VecTile<kBF16>::kUnpackSmemBytes : VecTile<kBF16>::kSmemBytes)
+           : (kUnpack ? T::kUnpackSmemBytes : T::kSmemBytes);
   constexpr int kTileRows = kVec ? kVecTileRows : kColTileRows;
   constexpr int kTileCols = kVec ? VecTile<kBF16>::kTileCols : kColTileCols;
   int dev = 0;
