@@ -1,5 +1,5 @@
 // mx_packed.cu -- MX9 and MX6 in one packed tensor, blocked along either axis
-// of a strided 2-D tensor, with a zero-padded partial last block.
+// of a 2-D tensor with strided rows, with a zero-padded partial last block.
 //
 // AMD-AGI/ALTO PR #33 "mx9: add fused MX9 quantization kernel with
 // pack/unpack": the later commits pack MX9 "into a single uint8 tensor",
@@ -12,18 +12,18 @@
 // 5-bit two's-complement codes, element i at bits 5i..5i+4 of the 10 data
 // bytes read as one little-endian number.
 //
-// A tensor blocked along its rows with whole blocks per row and 16-byte
-// aligned rows (the common case) is a run of whole blocks, row by row: packing
-// goes through the TMA-fed pack kernel of mx9.cu in its record form, and
-// unpacking through mx_unpack_records_kernel below, where a warp copies runs
-// of records into shared memory with 16-byte loads and each lane then writes
-// 16 output bytes.  Every other geometry (blocks along columns,
-// strided rows, partial blocks) takes the generic kernels: one thread owns one
-// block; along axis 1 (a row) a warp's 32 blocks are consecutive records,
-// staged in shared memory and moved with 16-byte coalesced copies; along axis
-// 0 (a column) the lanes of a warp take neighbouring columns, so every element
-// load and store is coalesced and each record is written with its own narrow
-// stores.
+// Kernels by geometry:
+// * blocked rows with whole blocks per row and 16-byte aligned rows (the
+//   common case): packing goes through the TMA-fed pack kernel of mx9.cu in
+//   its record form; unpacking through mx_unpack_records_kernel, where a warp
+//   copies runs of records into shared memory with 16-byte loads and each lane
+//   then writes 16 output bytes;
+// * blocks along columns: the column-tile kernels, a shared-memory transpose
+//   (vector tiles where rows move in 16-byte pieces, element tiles otherwise);
+// * any other blocked-row tensor (short strided rows, partial last blocks,
+//   unaligned pointers): the generic row kernels, one thread per block, a
+//   warp's 32 consecutive records staged in shared memory and moved with
+//   coalesced copies.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -47,110 +47,15 @@ struct Fmt {
   static constexpr int kQMax = kFmt == MXQ_FMT_MX9 ? 127 : 15;   // symmetric clamp
 };
 
+// A 2-D tensor: rows x cols elements, rows ld elements apart.
 struct Geometry {
   int64_t rows, cols, ld;
-  int axis;
-  __host__ __device__ int64_t lines() const { return axis == 1 ? rows : cols; }
-  __host__ __device__ int64_t len() const { return axis == 1 ? cols : rows; }
 };
-
-__device__ __forceinline__ int64_t elem_index(const Geometry& g, int64_t line, int64_t pos) {
-  return g.axis == 1 ? line * g.ld + pos : pos * g.ld + line;
-}
-
-// Work item w -> (line, j): along axis 1 consecutive work items are
-// consecutive blocks of a row; along axis 0 consecutive work items are the
-// same block position j of neighbouring columns.
-__device__ __forceinline__ void work_to_block(const Geometry& g, int64_t nbl, int64_t w,
-                                              int64_t* line, int64_t* j) {
-  if (g.axis == 1) {
-    *line = w / nbl;
-    *j = w - *line * nbl;
-  } else {
-    const int64_t lines = g.lines();
-    *j = w / lines;
-    *line = w - *j * lines;
-  }
-}
 
 template <bool kBF16>
 __device__ __forceinline__ uint32_t load_bits(const uint8_t* x, int64_t idx) {
   if (kBF16) return static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(x) + idx)) << 16;
   return __ldg(reinterpret_cast<const uint32_t*>(x) + idx);
-}
-
-// 2^-k for a pair: k = max(E - off - t, -126) with E = eb8 - 127, so
-// 127 - k = min(254 - eb8 + off + t, 253) (always a normal exponent field).
-template <int kOff>
-__device__ __forceinline__ float pair_mult(uint32_t eb8, uint32_t t) {
-  return __uint_as_float(min(254u + kOff - eb8 + t, 253u) << 23);
-}
-
-template <int kQMax>
-__device__ __forceinline__ int q_of(float x, float m) {
-  const int r = __float2int_rn(fmul_rn_noftz(x, m));  // NaN -> 0, +-Inf saturate
-  return max(-kQMax, min(kQMax, r));
-}
-
-// The block rule on 16 fp32 bit patterns (zero for padding): exponent byte,
-// prime byte and the 16 integer values.
-template <int kFmt>
-__device__ __forceinline__ void block_rule(const uint32_t* f, uint32_t* eb8_out, uint32_t* bits_out,
-                                           int* q) {
-  uint32_t pe[8], eb = 0;
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    pe[p] = max(f[2 * p] & 0x7F800000u, f[2 * p + 1] & 0x7F800000u);
-    eb = max(eb, pe[p]);
-  }
-  const uint32_t eb8 = eb >> 23;
-  uint32_t bits = 0;
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const uint32_t t = pe[p] < eb;
-    bits |= t << p;
-    const float m = pair_mult<Fmt<kFmt>::kOffset>(eb8, t);
-    q[2 * p] = q_of<Fmt<kFmt>::kQMax>(__uint_as_float(f[2 * p]), m);
-    q[2 * p + 1] = q_of<Fmt<kFmt>::kQMax>(__uint_as_float(f[2 * p + 1]), m);
-  }
-  *eb8_out = eb8;
-  *bits_out = bits;
-}
-
-// Record bytes as 32-bit words (the MX9 record's last word holds 2 bytes).
-template <int kFmt>
-__device__ __forceinline__ void encode_record(uint32_t eb8, uint32_t bits, const int* q,
-                                              uint32_t* w) {
-  const uint32_t head = eb8 | (bits << 8);
-  if (kFmt == MXQ_FMT_MX9) {
-    uint32_t b[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) b[i] = static_cast<uint32_t>(q[i]) & 0xFFu;
-    w[0] = head | (b[0] << 16) | (b[1] << 24);
-#pragma unroll
-    for (int k = 1; k < 4; ++k)
-      w[k] = b[4 * k - 2] | (b[4 * k - 1] << 8) | (b[4 * k] << 16) | (b[4 * k + 1] << 24);
-    w[4] = b[14] | (b[15] << 8);
-  } else {
-    uint64_t lo = 0;
-    uint32_t hi = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint64_t code = static_cast<uint64_t>(static_cast<uint32_t>(q[i]) & 0x1Fu);
-      const int s = 5 * i;
-      if (s + 5 <= 64) {
-        lo |= code << s;
-      } else if (s >= 64) {
-        hi |= static_cast<uint32_t>(code << (s - 64));
-      } else {
-        lo |= code << s;
-        hi |= static_cast<uint32_t>(code >> (64 - s));
-      }
-    }
-    w[0] = head | (static_cast<uint32_t>(lo & 0xFFFFu) << 16);
-    w[1] = static_cast<uint32_t>(lo >> 16);
-    w[2] = static_cast<uint32_t>(lo >> 48) | (hi << 16);
-  }
 }
 
 template <int kFmt>
@@ -189,40 +94,6 @@ __device__ __forceinline__ void decode_record(const uint32_t* w, uint32_t* eb8, 
   }
 }
 
-template <int kFmt>
-__device__ __forceinline__ void store_record_narrow(uint8_t* dst, const uint32_t* w) {
-  if (kFmt == MXQ_FMT_MX9) {  // 18 bytes, 2-byte aligned
-    uint16_t* h = reinterpret_cast<uint16_t*>(dst);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      h[2 * k] = static_cast<uint16_t>(w[k] & 0xFFFFu);
-      h[2 * k + 1] = static_cast<uint16_t>(w[k] >> 16);
-    }
-    h[8] = static_cast<uint16_t>(w[4] & 0xFFFFu);
-  } else {  // 12 bytes, 4-byte aligned
-    uint32_t* p = reinterpret_cast<uint32_t*>(dst);
-    p[0] = w[0];
-    p[1] = w[1];
-    p[2] = w[2];
-  }
-}
-
-template <int kFmt>
-__device__ __forceinline__ void load_record_narrow(const uint8_t* src, uint32_t* w) {
-  if (kFmt == MXQ_FMT_MX9) {
-    const uint16_t* h = reinterpret_cast<const uint16_t*>(src);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      w[k] = static_cast<uint32_t>(__ldg(h + 2 * k)) | (static_cast<uint32_t>(__ldg(h + 2 * k + 1)) << 16);
-    w[4] = __ldg(h + 8);
-  } else {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(src);
-    w[0] = __ldg(p);
-    w[1] = __ldg(p + 1);
-    w[2] = __ldg(p + 2);
-  }
-}
-
 // Copy `bytes` between global and a warp's 16-byte aligned shared staging
 // area (global side 16-byte aligned when `aligned`, else byte by byte).
 __device__ __forceinline__ void warp_copy_out(uint8_t* g, const uint8_t* s, int bytes, bool aligned,
@@ -249,28 +120,29 @@ __device__ __forceinline__ void warp_copy_in(uint8_t* s, const uint8_t* g, int b
   }
 }
 
+// Generic blocked-row kernels: rows of g.cols elements (partial last block
+// zero-padded), g.ld apart.  Work item w is block j = w % nbl of row w / nbl,
+// i.e. record w.  vec_rows: x (or y) and ld allow 16-byte element access.
 template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_pack_packed_kernel(const uint8_t* __restrict__ x, Geometry g, bool vec_rows,
                           bool packed_aligned, uint8_t* __restrict__ packed) {
+  using R = MxRule<Fmt<kFmt>::kOffset, Fmt<kFmt>::kQMax>;
   constexpr int RB = Fmt<kFmt>::kRecord;
   __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t nbl = (g.len() + 15) / 16;
-  const int64_t nb = g.lines() * nbl;
+  const int64_t nbl = (g.cols + 15) / 16;
+  const int64_t nb = g.rows * nbl;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kThreads + warp * 32; w0 < nb; w0 += stride) {
     const int64_t w = w0 + lane;  // warp-uniform loop; lanes past nb idle
-    uint32_t rec[5] = {0, 0, 0, 0, 0};
-    int64_t b = 0;
     if (w < nb) {
-      int64_t line, j;
-      work_to_block(g, nbl, w, &line, &j);
-      b = line * nbl + j;
-      const int64_t valid = min(static_cast<int64_t>(16), g.len() - 16 * j);
+      const int64_t row = w / nbl, j = w - row * nbl;
+      const int64_t valid = min(static_cast<int64_t>(16), g.cols - 16 * j);
+      const int64_t e0 = row * g.ld + 16 * j;  // first element of the block
       uint32_t f[16];
-      if (g.axis == 1 && vec_rows && valid == 16) {
-        const uint8_t* src = x + elem_index(g, line, 16 * j) * (kBF16 ? 2 : 4);
+      if (vec_rows && valid == 16) {
+        const uint8_t* src = x + e0 * (kBF16 ? 2 : 4);
         if (kBF16) {
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -278,7 +150,7 @@ __global__ void __launch_bounds__(kThreads)
             const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              f[8 * k + 2 * i] = wd[i] << 16;
+              f[8 * k + 2 * i] = wd[i] << 16;  // exact widening
               f[8 * k + 2 * i + 1] = wd[i] & 0xFFFF0000u;
             }
           }
@@ -294,32 +166,17 @@ __global__ void __launch_bounds__(kThreads)
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          f[i] = i < valid ? load_bits<kBF16>(x, elem_index(g, line, 16 * j + i)) : 0u;
+        for (int i = 0; i < 16; ++i) f[i] = i < valid ? load_bits<kBF16>(x, e0 + i) : 0u;
       }
-      uint32_t eb8, bits;
-      int q[16];
-      block_rule<kFmt>(f, &eb8, &bits, q);
-      encode_record<kFmt>(eb8, bits, q, rec);
+      uint32_t h[8], eb8, bits;
+      R::block_f32(f, h, &eb8, &bits);
+      stage_record<kFmt>(smem_u32(stage[warp]) + static_cast<uint32_t>(lane) * RB, eb8, bits, h);
     }
-    if (g.axis == 1) {
-      // the warp's records b = w0 .. w0+31 are contiguous: stage and copy out
-      uint8_t* st = stage[warp];
-      if (w < nb) {
-        uint16_t* h = reinterpret_cast<uint16_t*>(st + lane * RB);
-#pragma unroll
-        for (int k = 0; k < (RB + 3) / 4; ++k) {
-          h[2 * k] = static_cast<uint16_t>(rec[k] & 0xFFFFu);
-          if (4 * k + 2 < RB) h[2 * k + 1] = static_cast<uint16_t>(rec[k] >> 16);
-        }
-      }
-      __syncwarp();
-      const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
-      warp_copy_out(packed + w0 * RB, st, static_cast<int>(nvalid) * RB, packed_aligned, lane);
-      __syncwarp();
-    } else if (w < nb) {
-      store_record_narrow<kFmt>(packed + b * RB, rec);
-    }
+    // the warp's records w0 .. w0+31 are contiguous
+    __syncwarp();
+    const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
+    warp_copy_out(packed + w0 * RB, stage[warp], static_cast<int>(nvalid) * RB, packed_aligned, lane);
+    __syncwarp();
   }
 }
 
@@ -330,31 +187,27 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int RB = Fmt<kFmt>::kRecord;
   __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t nbl = (g.len() + 15) / 16;
-  const int64_t nb = g.lines() * nbl;
+  const int64_t nbl = (g.cols + 15) / 16;
+  const int64_t nb = g.rows * nbl;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kThreads + warp * 32; w0 < nb; w0 += stride) {
     const int64_t w = w0 + lane;
     uint32_t rec[5] = {0, 0, 0, 0, 0};
-    if (g.axis == 1) {
-      uint8_t* st = stage[warp];
-      const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
-      warp_copy_in(st, packed + w0 * RB, static_cast<int>(nvalid) * RB, packed_aligned, lane);
-      __syncwarp();
-      if (w < nb) {
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(st + lane * RB);
+    uint8_t* st = stage[warp];
+    const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
+    warp_copy_in(st, packed + w0 * RB, static_cast<int>(nvalid) * RB, packed_aligned, lane);
+    __syncwarp();
+    if (w < nb) {
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(st + lane * RB);
 #pragma unroll
-        for (int k = 0; k < (RB + 3) / 4; ++k)
-          rec[k] = static_cast<uint32_t>(h[2 * k]) |
-                   (4 * k + 2 < RB ? static_cast<uint32_t>(h[2 * k + 1]) << 16 : 0u);
-      }
-      __syncwarp();
+      for (int k = 0; k < (RB + 3) / 4; ++k)
+        rec[k] = static_cast<uint32_t>(h[2 * k]) |
+                 (4 * k + 2 < RB ? static_cast<uint32_t>(h[2 * k + 1]) << 16 : 0u);
     }
+    __syncwarp();
     if (w >= nb) continue;
-    int64_t line, j;
-    work_to_block(g, nbl, w, &line, &j);
-    const int64_t b = line * nbl + j;
-    if (g.axis != 1) load_record_narrow<kFmt>(packed + b * RB, rec);
+    const int64_t row = w / nbl, j = w - row * nbl;
+    const int64_t e0 = row * g.ld + 16 * j;
     uint32_t eb8, bits;
     int q[16];
     decode_record<kFmt>(rec, &eb8, &bits, q);
@@ -362,21 +215,20 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t t = (bits >> (i / 2)) & 1u;
-      // 2^k, k = max(E - off - t, -126): exponent field min(eb8 - off - t, 127 - 126)
+      // 2^k, k = max(E - off - t, -126): exponent field max(eb8 - off - t, 1)
       const int kf = max(static_cast<int>(eb8) - Fmt<kFmt>::kOffset - static_cast<int>(t), 1);
       v[i] = fmul_rn_noftz(static_cast<float>(q[i]), __uint_as_float(static_cast<uint32_t>(kf) << 23));
     }
-    const int64_t valid = min(static_cast<int64_t>(16), g.len() - 16 * j);
-    if (g.axis == 1 && vec_rows && valid == 16) {
-      uint8_t* dst = y + elem_index(g, line, 16 * j) * (kBF16 ? 2 : 4);
+    const int64_t valid = min(static_cast<int64_t>(16), g.cols - 16 * j);
+    if (vec_rows && valid == 16) {
+      uint8_t* dst = y + e0 * (kBF16 ? 2 : 4);
       if (kBF16) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           uint32_t wd[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            wd[i] = (__float_as_uint(v[8 * k + 2 * i]) >> 16) |
-                    (__float_as_uint(v[8 * k + 2 * i + 1]) & 0xFFFF0000u);
+            wd[i] = __byte_perm(__float_as_uint(v[8 * k + 2 * i]), __float_as_uint(v[8 * k + 2 * i + 1]), 0x7632);
           reinterpret_cast<uint4*>(dst)[k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
       } else {
@@ -389,11 +241,10 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         if (i >= valid) break;
-        const int64_t idx = elem_index(g, line, 16 * j + i);
         if (kBF16)
-          reinterpret_cast<uint16_t*>(y)[idx] = static_cast<uint16_t>(__float_as_uint(v[i]) >> 16);
+          reinterpret_cast<uint16_t*>(y)[e0 + i] = static_cast<uint16_t>(__float_as_uint(v[i]) >> 16);
         else
-          reinterpret_cast<float*>(y)[idx] = v[i];
+          reinterpret_cast<float*>(y)[e0 + i] = v[i];
       }
     }
   }
@@ -1107,7 +958,7 @@ extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t co
     return launch_records_pack(x, dtype == MXQ_BF16, fmt, nb, cols / 16,
                                (rows == 1 ? cols : ld) * esize, packed, stream);
   }
-  const Geometry g{rows, cols, ld, axis};
+  const Geometry g{rows, cols, ld};
   if (axis == 0) {
     const uint8_t* xc = static_cast<const uint8_t*>(x);
     const bool pa = aligned_to(packed, 16);
@@ -1157,7 +1008,7 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
                ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb)
                : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb);
   }
-  const Geometry g{rows, cols, ld, axis};
+  const Geometry g{rows, cols, ld};
   if (axis == 0) {
     const bool pa = aligned_to(packed, 16);
     if (cols_vec_ok(y, dtype, cols, ld)) {
