@@ -99,6 +99,33 @@ int mxq_quantize_2d_dual(const void *x, int64_t M, int64_t N, const int32_t *off
                          cudaStream_t stream);
 
 /*
+ * The same cast on a band of rows [row0, row0 + rows) of a full [M, N] tensor,
+ * for data-parallel shards along M.  The pages' tiles and blocks are
+ * independent, so the band's outputs are exactly the full call's bytes at the
+ * band's places; only s_col needs the band's position, because a group's slab
+ * offset and width come from the full tensor's offs.
+ *
+ *   x      bf16 [rows, N]: the band (row0 .. row0+rows-1 of the full tensor).
+ *   rows, row0, M, N   multiples of 128 with row0 + rows <= M; rows == 0 is a
+ *          no-op.
+ *   offs, G  the full tensor's K-group offsets (as for mxq_quantize_2d_dual,
+ *          checked on the device against M); NULL and 0 for dense.
+ *   q_row  E4M3 [rows*N]: rows row0.. of the full q_row.
+ *   s_row  E8M0 [rows*N/32]: bytes [row0*N/32, (row0+rows)*N/32) of the full
+ *          s_row (the blocked layout keeps a band of 128-row blocks together).
+ *   q_col  E4M3 [N*rows]: [N, rows] row-major, columns row0.. of the full q_col.
+ *   s_col  E8M0 [N*M/32]: the FULL colwise scale buffer; the call writes the
+ *          512-byte atoms of its rows (and the zero atoms of its tail rows) and
+ *          leaves every other byte alone, so bands that cover [0, M) once write
+ *          every byte once, with no exchange between them.
+ * Errors and device status as for mxq_quantize_2d_dual; MXQ_EBADSHAPE also for
+ * a band outside [0, M).
+ */
+int mxq_quantize_2d_dual_rows(const void *x, int64_t rows, int64_t N, int64_t row0, int64_t M,
+                              const int32_t *offs, int32_t G, uint8_t *q_row, uint8_t *s_row,
+                              uint8_t *q_col, uint8_t *s_col, cudaStream_t stream);
+
+/*
  * MX9 pack.  [MX9] Summary / "Key design choices": blocks of 16 consecutive
  * elements along the last axis (block b = r*(cols/16) + j); per block a
  * shared exponent E = max over the block of the element exponents taken from

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
         L.mxq_quantize_2d_dual.restype = ctypes.c_int
         L.mxq_quantize_2d_dual.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+        L.mxq_quantize_2d_dual_rows.restype = ctypes.c_int
+        L.mxq_quantize_2d_dual_rows.argtypes = [vp, i64, i64, i64, i64, vp, i32, vp, vp, vp, vp, vp]
         L.mx9_pack.restype = ctypes.c_int
         L.mx9_pack.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, vp, vp]
         L.mx9_unpack.restype = ctypes.c_int
@@ -191,6 +193,48 @@ def quantize_2d_dual(x, offs=None, *, out: Optional[DualOutputs] = None, stream=
     if rc != OK:
         raise MxqError(rc, "mxq_quantize_2d_dual")
     return out
+
+
+def quantize_2d_dual_rows(x, row0: int, M: int, s_col, offs=None, *, out=None, stream=None):
+    """The dual-axis cast of rows [row0, row0 + x.shape[0]) of a full [M, N]
+    tensor (a data-parallel band along M).  ``s_col`` is the FULL colwise
+    scale buffer (uint8, N*M/32): this call writes the band's atoms only.
+    ``offs`` are the full tensor's group ends.  Returns the band's q_row,
+    s_row and q_col (q_col as [N, rows]) and s_col."""
+    torch = _torch()
+    _check_cuda(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    rows, N = x.shape
+    G = 0
+    if offs is not None:
+        _check_cuda(offs, "offs")
+        if offs.dtype != torch.int32 or offs.dim() != 1 or offs.device != x.device:
+            raise ValueError("offs must be a 1-D int32 tensor on x's device")
+        G = offs.numel()
+    _check_cuda(s_col, "s_col")
+    if s_col.dtype != torch.uint8 or s_col.numel() != N * M // 32 or s_col.device != x.device:
+        raise ValueError("s_col must be the full uint8 colwise scale buffer (N*M/32) on x's device")
+    if out is None:
+        kw = dict(dtype=torch.uint8, device=x.device)
+        out = (torch.empty((rows, N), **kw), torch.empty((rows * N // 32,), **kw),
+               torch.empty((N, rows), **kw))
+    q_row, s_row, q_col = out
+    for name, t, n in (("q_row", q_row, rows * N), ("s_row", s_row, rows * N // 32),
+                       ("q_col", q_col, rows * N)):
+        _check_cuda(t, name)
+        if t.dtype != torch.uint8 or t.numel() != n or t.device != x.device:
+            raise ValueError(f"{name} must be a uint8 tensor of {n} elements on x's device")
+    with torch.cuda.device(x.device):
+        rc = lib().mxq_quantize_2d_dual_rows(
+            ctypes.c_void_p(x.data_ptr()), rows, N, row0, M,
+            ctypes.c_void_p(offs.data_ptr() if offs is not None else 0), G,
+            ctypes.c_void_p(q_row.data_ptr()), ctypes.c_void_p(s_row.data_ptr()),
+            ctypes.c_void_p(q_col.data_ptr()), ctypes.c_void_p(s_col.data_ptr()),
+            _stream_handle(x.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_quantize_2d_dual_rows")
+    return DualOutputs(q_row, s_row, q_col, s_col)
 
 
 def _check_x_offs(x, offs):

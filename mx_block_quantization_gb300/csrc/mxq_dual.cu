@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
     mxq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_qrow,
                     const __grid_constant__ CUtensorMap tm_qcol, const int32_t* __restrict__ offs,
-                    int G, int M, int N, uint8_t* __restrict__ s_row,
+                    int G, int M, int N, int grow0, int Mtot, uint8_t* __restrict__ s_row,
                     uint8_t* __restrict__ s_col) {
   using R = Roles<kMode>;
   extern __shared__ uint8_t smem_raw[];
@@ -340,15 +340,16 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
   }
 
   // Device-side check of the group offsets (fused cast only): ascending,
-  // multiples of 128, within [0, M].  Every CTA reaches the same verdict; on
-  // failure nothing is written and the status word records it.
-  int64_t end_rows = M;
+  // multiples of 128, within [0, Mtot] (the full tensor's rows; this launch
+  // casts its rows [grow0, grow0 + M)).  Every CTA reaches the same verdict;
+  // on failure nothing is written and the status word records it.
+  int64_t end_rows = Mtot;
   if (kMode == kDual && offs != nullptr) {
     int bad = 0;
     for (int g = tid; g < G; g += R::kThreads) {
       const int32_t v = offs[g];
       const int32_t prev = g ? offs[g - 1] : 0;
-      if (v < prev || (v & (kTile - 1)) != 0 || v > M) bad = 1;
+      if (v < prev || (v & (kTile - 1)) != 0 || v > Mtot) bad = 1;
       s_offs[g] = v;
     }
     bad = __syncthreads_or(bad);
@@ -452,20 +453,21 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
                          base + kOffQCol + b * kQTileBytes);
         }
         if (kMode == kDual) {
-          if (row0 < end_rows) {
-            int64_t lo = 0, hi = Mrows;
+          const int64_t grow = grow0 + row0;  // the tile's first row in the full tensor
+          if (grow < end_rows) {
+            int64_t lo = 0, hi = Mtot;
             if (offs != nullptr) {
-              const int g = group_of_row(s_offs, G, row0);
+              const int g = group_of_row(s_offs, G, grow);
               lo = g ? s_offs[g - 1] : 0;
               hi = s_offs[g];
             }
             const int64_t atoms_per_nblock = (hi - lo) / kTile;  // (hi-lo)/32 scale cols / 4
             uint8_t* dst = s_col + static_cast<int64_t>(N) * lo / 32 +
-                           (tj * atoms_per_nblock + (row0 - lo) / kTile) * kAtomBytes;
+                           (tj * atoms_per_nblock + (grow - lo) / kTile) * kAtomBytes;
             bulk_store(dst, base + kOffSCol + b * kAtomBytes, kAtomBytes);
           } else {
             uint8_t* dst = s_col + static_cast<int64_t>(N) * end_rows / 32 +
-                           (((row0 - end_rows) / kTile) * TN + tj) * kAtomBytes;
+                           (((grow - end_rows) / kTile) * TN + tj) * kAtomBytes;
             bulk_store(dst, base + kOffZero, kAtomBytes);
           }
         }
@@ -534,7 +536,8 @@ int check_shape(int64_t M, int64_t N) {
 template <int kMode>
 int launch_tiles(const void* x, int64_t M, int64_t N, const int32_t* offs, int32_t G,
                  uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, int64_t grow0 = 0, int64_t Mtot = -1) {
+  if (Mtot < 0) Mtot = M;
   int dev = 0;
   const int sms = sm_count_current_device(&dev);
   if (sms <= 0 || !ensure_smem_attr<kMode>(dev)) return MXQ_ECUDA;
@@ -561,7 +564,8 @@ int launch_tiles(const void* x, int64_t M, int64_t N, const int32_t* offs, int32
   cfg.stream = stream;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, mxq_tile_kernel<kMode>, tm_x, tm_qrow, tm_qcol, offs,
-                         static_cast<int>(G), static_cast<int>(M), static_cast<int>(N), s_row, s_col);
+                         static_cast<int>(G), static_cast<int>(M), static_cast<int>(N),
+                         static_cast<int>(grow0), static_cast<int>(Mtot), s_row, s_col);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 
@@ -590,6 +594,36 @@ extern "C" int mxq_quantize_2d_dual(const void* x, int64_t M, int64_t N, const i
   };
   if (ranges_overlap(r, 6)) return MXQ_EOVERLAP;
   return launch_tiles<kDual>(x, M, N, offs, G, q_row, s_row, q_col, s_col, stream);
+}
+
+extern "C" int mxq_quantize_2d_dual_rows(const void* x, int64_t rows, int64_t N, int64_t row0,
+                                         int64_t M, const int32_t* offs, int32_t G, uint8_t* q_row,
+                                         uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                         cudaStream_t stream) {
+  int rc = check_shape(rows, N);
+  if (rc != MXQ_OK) return rc;
+  rc = check_shape(M, N);
+  if (rc != MXQ_OK) return rc;
+  if (row0 < 0 || row0 % kTile != 0 || row0 + rows > M) return MXQ_EBADSHAPE;
+  if (offs == nullptr ? G != 0 : (G < 1 || G > MXQ_MAX_GROUPS)) return MXQ_EBADOFFS;
+  if (offs != nullptr && !aligned_to(offs, 4)) return MXQ_EALIGN;
+  if (rows == 0 || N == 0) return MXQ_OK;
+  if (!x || !q_row || !s_row || !q_col || !s_col) return MXQ_ENULL;
+  if (!aligned_to(x, 16) || !aligned_to(q_row, 16) || !aligned_to(s_row, 16) ||
+      !aligned_to(q_col, 16) || !aligned_to(s_col, 16))
+    return MXQ_EALIGN;
+  const uint64_t RN = static_cast<uint64_t>(rows) * static_cast<uint64_t>(N);
+  const uint64_t MN = static_cast<uint64_t>(M) * static_cast<uint64_t>(N);
+  const ByteRange r[6] = {
+      {reinterpret_cast<uintptr_t>(x), 2 * RN},
+      {reinterpret_cast<uintptr_t>(q_row), RN},
+      {reinterpret_cast<uintptr_t>(q_col), RN},
+      {reinterpret_cast<uintptr_t>(s_row), RN / 32},
+      {reinterpret_cast<uintptr_t>(s_col), MN / 32},
+      {reinterpret_cast<uintptr_t>(offs), offs ? 4ull * static_cast<uint64_t>(G) : 0ull},
+  };
+  if (ranges_overlap(r, 6)) return MXQ_EOVERLAP;
+  return launch_tiles<kDual>(x, rows, N, offs, G, q_row, s_row, q_col, s_col, stream, row0, M);
 }
 
 extern "C" int mxq_quantize_1x32(const void* x, int64_t M, int64_t N, uint8_t* q_row,

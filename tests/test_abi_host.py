@@ -173,3 +173,26 @@ def test_packed_variant_rejections(L):
     assert pack(rows=0) == mxq.OK
     assert L.mx_unpack_packed(vp(A), 6, vp(A + 64), 0, 4, 32, 32, 1, None) == mxq.EOVERLAP
     assert L.mx_unpack_packed(vp(A + 2), 6, vp(A + 4096), 0, 4, 32, 32, 1, None) == mxq.EALIGN
+
+
+def test_dual_rows_rejections_before_any_cuda_call(L):
+    """The band entry checks its band, pointers and overlaps on the host."""
+    vp = ctypes.c_void_p
+    f = L.mxq_quantize_2d_dual_rows
+    N, M, rows = 128, 512, 128
+    RN = rows * N
+    x, qr, sr, qc, sc = A, A + 4 * RN, A + 8 * RN, A + 12 * RN, A + 16 * RN
+
+    def call(rows=rows, row0=0, M=M, x=x, qr=qr, sr=sr, qc=qc, sc=sc, offs=None, G=0):
+        return f(vp(x), rows, N, row0, M, vp(offs), G, vp(qr), vp(sr), vp(qc), vp(sc), None)
+
+    assert call(row0=64) == mxq.EBADSHAPE           # band start not a multiple of 128
+    assert call(row0=512) == mxq.EBADSHAPE          # band past the tensor
+    assert call(rows=256, row0=384) == mxq.EBADSHAPE
+    assert call(M=500) == mxq.EBADSHAPE
+    assert call(rows=0) == mxq.OK                    # empty band: nothing to do
+    assert call(x=0) == mxq.ENULL
+    assert call(qc=qc + 8) == mxq.EALIGN
+    assert call(sc=x + 64) == mxq.EOVERLAP           # the full s_col overlapping x
+    assert call(offs=A + 32 * RN, G=0) == mxq.EBADOFFS
+    assert call(offs=None, G=3) == mxq.EBADOFFS
