@@ -55,10 +55,16 @@ using namespace mxq;
 #define MXQ_MX9_REC_F32_RING_KB 96
 #endif
 #ifndef MXQ_MX9_REC_BF16_WARPS
-#define MXQ_MX9_REC_BF16_WARPS 16
+#define MXQ_MX9_REC_BF16_WARPS 8
 #endif
 #ifndef MXQ_MX9_REC_BF16_RING_KB
 #define MXQ_MX9_REC_BF16_RING_KB 64
+#endif
+#ifndef MXQ_MX9_REC_F32_PER_THREAD
+#define MXQ_MX9_REC_F32_PER_THREAD 1
+#endif
+#ifndef MXQ_MX9_REC_BF16_PER_THREAD
+#define MXQ_MX9_REC_BF16_PER_THREAD 4
 #endif
 #ifndef MXQ_MX9_PACK_CTAS_PER_SM
 #define MXQ_MX9_PACK_CTAS_PER_SM 2
@@ -101,7 +107,9 @@ struct PackShape {
   static constexpr int kWarps =
       kOut == kSplit ? (kBF16 ? MXQ_MX9_PACK_BF16_WARPS : MXQ_MX9_PACK_F32_WARPS)
                      : (kBF16 ? MXQ_MX9_REC_BF16_WARPS : MXQ_MX9_REC_F32_WARPS);
-  static constexpr int kPerThread = kBF16 ? MXQ_MX9_PACK_BF16_PER_THREAD : MXQ_MX9_PACK_F32_PER_THREAD;
+  static constexpr int kPerThread =
+      kOut == kSplit ? (kBF16 ? MXQ_MX9_PACK_BF16_PER_THREAD : MXQ_MX9_PACK_F32_PER_THREAD)
+                     : (kBF16 ? MXQ_MX9_REC_BF16_PER_THREAD : MXQ_MX9_REC_F32_PER_THREAD);
   static constexpr int kThreads = (kWarps + 1) * 32;
   static constexpr int kConsumers = kWarps * 32;
   static constexpr int kBlocksPerStage = kConsumers * kPerThread;
@@ -117,10 +125,12 @@ struct PackShape {
   static constexpr uint32_t kOffBar = kStages * kStageBytes;
   static constexpr uint32_t kOffFlag = kOffBar + 16u * kStages;
   static constexpr uint32_t kOffRec = kOffFlag + 16u;
-  static constexpr uint32_t kRunBytes = 32u * kRecord;  // one warp's 32 records
-  static constexpr uint32_t kSmemBytes = kOffRec + kWarps * 2u * kRunBytes + 128u;  // + alignment
+  // record outputs: a warp owns kPerThread * 32 consecutive blocks of a stage
+  static constexpr int kWarpBlocks = 32 * kPerThread;
+  static constexpr uint32_t kWarpRecBytes = kWarpBlocks * kRecord;
+  static constexpr uint32_t kSmemBytes = kOffRec + kWarps * 2u * kWarpRecBytes + 128u;  // + alignment
   static_assert(kStages >= 2, "ring too small");
-  static_assert((32u * kRecord) % 16u == 0, "record runs of a warp stay 16-byte aligned");
+  static_assert(kWarpRecBytes % 16u == 0, "record runs of a warp stay 16-byte aligned");
   static_assert(kSmemBytes * MXQ_MX9_PACK_CTAS_PER_SM <= 227u * 1024u, "shared memory budget");
 };
 
@@ -204,9 +214,10 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
   }
 
   // -------------------------------------------------------------- consumers
-  // Record outputs: two staging buffers per warp, alternating over its runs;
-  // a whole run leaves with one bulk store issued by lane 0.
-  const uint32_t rec_stage = base + S::kOffRec + static_cast<uint32_t>(warp) * 2u * S::kRunBytes;
+  // Record outputs: a warp takes kWarpBlocks consecutive blocks of each stage,
+  // stages their records in one of its two buffers (alternating over stages)
+  // and lane 0 writes them with one bulk store.
+  const uint32_t rec_stage = base + S::kOffRec + static_cast<uint32_t>(warp) * 2u * S::kWarpRecBytes;
   uint32_t runs = 0;
   for (int64_t i = 0; i < my; ++i) {
     const int s = static_cast<int>(i % S::kStages);
@@ -214,57 +225,67 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
                                       abort_flag, &g_mx9_status, MXQ_DEV_TIMEOUT);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     const int64_t blk0 = (blockIdx.x + i * static_cast<int64_t>(gridDim.x)) * S::kBlocksPerStage;
-#pragma unroll
-    for (int j = 0; j < S::kPerThread; ++j) {
-      const int local = j * S::kConsumers + tid;
-      const int64_t run0 = blk0 + (local - lane);  // this warp's 32 consecutive blocks
-      if (run0 >= nb) break;                       // warp-uniform
-      const int64_t blk = blk0 + local;
-      uint32_t h[8], eb8 = 0, bits = 0;
-      if (blk < nb) {
-        const uint32_t src =
-            base + static_cast<uint32_t>(s) * S::kStageBytes + local * S::kBlockBytes;
-        if (kBF16) {
-          const uint4 a = lds128(src), b = lds128(src + 16);
-          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-          R::block_bf16(w, h, &eb8, &bits);
-        } else {
-          uint32_t f[16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 a = lds128(src + 16u * k);
-            f[4 * k] = a.x;
-            f[4 * k + 1] = a.y;
-            f[4 * k + 2] = a.z;
-            f[4 * k + 3] = a.w;
-          }
-          R::block_f32(f, h, &eb8, &bits);
-        }
-      }
-      if (kOut == kSplit) {
-        if (blk < nb) {
-          __stcs(reinterpret_cast<uint4*>(q_or_rec) + blk, pairs_to_bytes(h));
-          max_exp[blk] = static_cast<uint8_t>(eb8);
-          prime[blk] = static_cast<uint8_t>(bits);
-        }
+    const uint32_t stage_base = base + static_cast<uint32_t>(s) * S::kStageBytes;
+    // 16-element block `local` of this stage -> its clamped int16 pairs
+    auto quantize = [&](int local, uint32_t* h, uint32_t* eb8, uint32_t* bits) {
+      const uint32_t src = stage_base + static_cast<uint32_t>(local) * S::kBlockBytes;
+      if (kBF16) {
+        const uint4 a = lds128(src), b = lds128(src + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        R::block_bf16(w, h, eb8, bits);
       } else {
-        const uint32_t buf = rec_stage + (runs & 1u) * S::kRunBytes;
+        uint32_t f[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 a = lds128(src + 16u * k);
+          f[4 * k] = a.x;
+          f[4 * k + 1] = a.y;
+          f[4 * k + 2] = a.z;
+          f[4 * k + 3] = a.w;
+        }
+        R::block_f32(f, h, eb8, bits);
+      }
+    };
+    if (kOut == kSplit) {
+#pragma unroll
+      for (int j = 0; j < S::kPerThread; ++j) {
+        const int local = j * S::kConsumers + tid;
+        const int64_t blk = blk0 + local;
+        if (blk >= nb) break;
+        uint32_t h[8], eb8, bits;
+        quantize(local, h, &eb8, &bits);
+        __stcs(reinterpret_cast<uint4*>(q_or_rec) + blk, pairs_to_bytes(h));
+        max_exp[blk] = static_cast<uint8_t>(eb8);
+        prime[blk] = static_cast<uint8_t>(bits);
+      }
+    } else {
+      const int64_t wrun0 = blk0 + static_cast<int64_t>(warp) * S::kWarpBlocks;
+      if (wrun0 < nb) {  // warp-uniform
+        const uint32_t buf = rec_stage + (runs & 1u) * S::kWarpRecBytes;
         ++runs;
         if (lane == 0) bulk_wait_read<1>();  // the store that last read buf is done with it
         __syncwarp();
-        if (blk < nb) stage_record<kOut>(buf + static_cast<uint32_t>(lane) * S::kRecord, eb8, bits, h);
-        const int64_t nvalid = nb - run0 < 32 ? nb - run0 : 32;
+#pragma unroll
+        for (int j = 0; j < S::kPerThread; ++j) {
+          const int r = j * 32 + lane;  // record of this warp's run
+          if (wrun0 + r < nb) {
+            uint32_t h[8], eb8, bits;
+            quantize(warp * S::kWarpBlocks + r, h, &eb8, &bits);
+            stage_record<kOut>(buf + static_cast<uint32_t>(r) * S::kRecord, eb8, bits, h);
+          }
+        }
+        const int64_t nvalid = nb - wrun0 < S::kWarpBlocks ? nb - wrun0 : S::kWarpBlocks;
         const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kRecord;
         if (bytes % 16u == 0) {
           fence_proxy_async_smem();  // staged records before the bulk store reads them
           __syncwarp();
           if (lane == 0) {
-            bulk_store(q_or_rec + run0 * S::kRecord, buf, bytes);
+            bulk_store(q_or_rec + wrun0 * S::kRecord, buf, bytes);
             bulk_commit();
           }
         } else {  // the tensor's last, partial run
           __syncwarp();
-          copy_records_out(q_or_rec + run0 * S::kRecord, buf, bytes, lane);
+          copy_records_out(q_or_rec + wrun0 * S::kRecord, buf, bytes, lane);
         }
       }
     }
