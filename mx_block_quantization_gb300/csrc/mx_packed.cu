@@ -617,9 +617,13 @@ struct VecTile {
   static constexpr uint32_t kUnpackSmemBytes = kVecTileBytes + kWarps * 2u * kStageBytes;
 };
 
-// Byte offset of word w (0..3) of piece p in row r of a vector tile.
-__device__ __forceinline__ uint32_t vec_word(int r, int p, int w) {
-  return static_cast<uint32_t>(r * (kVecPieces * 16) + ((p ^ ((r >> 4) & 7)) << 4) + 4 * w);
+// Word w (0..3) of piece p in row r of a vector tile sits at byte
+// r * kVecRowBytes + ((p ^ (r / 16 % 8)) << 4) + 4w.  Row i (0..15) of block j
+// is row 16j + i, so its swizzle is j's: vec_block_base(j, p, w) + i * kVecRowBytes.
+constexpr uint32_t kVecRowBytes = kVecPieces * 16;
+__device__ __forceinline__ uint32_t vec_block_base(int j, int p, int w) {
+  return static_cast<uint32_t>(16 * j) * kVecRowBytes + (static_cast<uint32_t>(p ^ (j & 7)) << 4) +
+         4u * static_cast<uint32_t>(w);
 }
 
 // Copy a run of staged records out (or in): 16-byte units when both sides allow it.
@@ -666,13 +670,15 @@ __global__ void __launch_bounds__(kThreads)
     const bool piece_ok = c0 + lane * V::kColsPerPiece < g.cols;
     // rows in: 16 per warp, each lane's pieces copied asynchronously straight
     // to their swizzled places (zero-filled outside the tensor)
+    static_assert(kWarps == 8, "row warp + 8k lies in block k / 2");
+    const uint8_t* xrow = x + ((r0 + warp) * g.ld + c0 + lane * V::kColsPerPiece) * esize;
 #pragma unroll
     for (int k = 0; k < kVecTileRows / kWarps; ++k) {
       const int r = warp + kWarps * k;
-      const int64_t row = r0 + r;
-      const bool in = piece_ok && row < g.rows;
-      const uint8_t* src = in ? x + (row * g.ld + c0 + lane * V::kColsPerPiece) * esize : x;
-      cp_async_16(tile + vec_word(r, lane, 0), src, in ? 16u : 0u);
+      const bool in = piece_ok && r0 + r < g.rows;
+      const uint32_t dst = tile + static_cast<uint32_t>(r) * kVecRowBytes +
+                           (static_cast<uint32_t>(lane ^ ((k >> 1) & 7)) << 4);
+      cp_async_16(dst, in ? xrow + static_cast<int64_t>(kWarps * k) * g.ld * esize : x, in ? 16u : 0u);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -683,7 +689,9 @@ __global__ void __launch_bounds__(kThreads)
       if (c0 + static_cast<int64_t>(pg) * V::kColsPerPiece >= g.cols) break;  // warp-uniform
       uint32_t wd[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) wd[i] = lds32(tile + vec_word(16 * j + i, pg, wsub));
+      const uint32_t col = tile + vec_block_base(j, pg, wsub);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) wd[i] = lds32(col + i * kVecRowBytes);
       if (j < nvalid) {
         uint32_t h[8], eb8, bits;
         if (kBF16) {
@@ -838,18 +846,20 @@ __global__ void __launch_bounds__(kThreads)
           for (int i = 0; i < 16; ++i) wd[i] = __float_as_uint(a[i]);
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sts32(tile + vec_word(16 * j + i, pg, wsub), wd[i]);
+        for (int i = 0; i < 16; ++i) sts32(tile + vec_block_base(j, pg, wsub) + i * kVecRowBytes, wd[i]);
       }
       __syncwarp();  // slot k & 1 is refilled at step k + 2
     }
     __syncthreads();
     const bool piece_ok = c0 + lane * V::kColsPerPiece < g.cols;
-#pragma unroll 8
-    for (int r = warp; r < kVecTileRows; r += kWarps) {
-      const int64_t row = r0 + r;
-      if (!piece_ok || row >= g.rows) continue;
-      const uint4 v = lds128(tile + vec_word(r, lane, 0));
-      __stcs(reinterpret_cast<uint4*>(y + (row * g.ld + c0 + lane * V::kColsPerPiece) * esize), v);
+    uint8_t* yrow = y + ((r0 + warp) * g.ld + c0 + lane * V::kColsPerPiece) * esize;
+#pragma unroll
+    for (int k = 0; k < kVecTileRows / kWarps; ++k) {
+      const int r = warp + kWarps * k;
+      if (!piece_ok || r0 + r >= g.rows) continue;
+      const uint4 v = lds128(tile + static_cast<uint32_t>(r) * kVecRowBytes +
+                             (static_cast<uint32_t>(lane ^ ((k >> 1) & 7)) << 4));
+      __stcs(reinterpret_cast<uint4*>(yrow + static_cast<int64_t>(kWarps * k) * g.ld * esize), v);
     }
     __syncthreads();
   }
