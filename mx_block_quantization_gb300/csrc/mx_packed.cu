@@ -685,10 +685,8 @@ __global__ void __launch_bounds__(kThreads)
     const int nvalid = static_cast<int>(nbl - tr * 8 < 8 ? nbl - tr * 8 : 8);
     const int j = lane >> 2, wsub = lane & 3;
     for (int pg = warp; pg < kVecPieces; pg += kWarps) {
-      const int64_t colw = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + wsub * (kBF16 ? 2 : 1);
       if (c0 + static_cast<int64_t>(pg) * V::kColsPerPiece >= g.cols) break;  // warp-uniform
       uint32_t wd[16];
-#pragma unroll
       const uint32_t col = tile + vec_block_base(j, pg, wsub);
 #pragma unroll
       for (int i = 0; i < 16; ++i) wd[i] = lds32(col + i * kVecRowBytes);
@@ -725,7 +723,6 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
       __syncwarp();
-      (void)colw;
     }
     __syncthreads();
   }
