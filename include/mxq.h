@@ -178,8 +178,12 @@ int mx9_unpack(const int8_t *q, const uint8_t *max_exp, const uint8_t *prime, vo
  * 16j..16j+15 (the tensor with the blocked axis moved last).  A partial last
  * block is zero-padded and then follows the normal rule; unpack writes only
  * the tensor's own elements.  packed: n_blocks * record bytes, 2-byte (MX9) or
- * 4-byte (MX6) aligned (16-byte alignment is faster).  Shape and axis are not
- * stored: the caller passes them back to unpack.
+ * 4-byte (MX6) aligned.  Any allowed alignment gives the same bytes; 16-byte
+ * aligned packed, x and row pitch (ld * element size) select the faster
+ * kernels.  Shape and axis are not stored: the caller passes them back to
+ * unpack.  Errors: MXQ_EBADDTYPE (dtype or fmt), MXQ_EBADSHAPE (negative
+ * sizes, ld < cols, axis not 0/1), MXQ_ENULL, MXQ_EALIGN (x not element-
+ * aligned, packed below the sizes above), MXQ_EOVERLAP, MXQ_ECUDA.
  */
 #define MXQ_FMT_MX9 9
 #define MXQ_FMT_MX6 6
