@@ -88,3 +88,31 @@ def test_mx9_past_2_31_elements():
         ry = oracle.mx9_unpack(rq, re, rp, "f32", 1, cols)
         assert_bytes_equal(y[r].cpu().view(torch.int32).numpy().view(np.uint8),
                            ry.view(np.uint8), f"row {r} unpack")
+
+
+@pytest.mark.parametrize("axis", [1, 0])
+def test_packed_mx9_past_2_31_elements(axis):
+    rows, cols = 131072, 16400
+    g = torch.Generator(device="cuda").manual_seed(23)
+    x = torch.randn(rows, cols, device="cuda", generator=g)
+    rec = mxq.mx_pack_packed(x, mxq.FMT_MX9, axis)
+    y = torch.empty_like(x)
+    mxq.mx_unpack_packed(rec, mxq.FMT_MX9, y, axis)
+    torch.cuda.synchronize()
+    if axis == 1:
+        bpl = cols // 16
+        for r in (0, rows // 2, rows - 1):
+            want = oracle.mx_pack(x[r:r + 1].cpu().numpy(), mxq.FMT_MX9, axis=1)
+            assert_bytes_equal(rec[r * bpl:(r + 1) * bpl].cpu().numpy(), want, f"row {r} records")
+            ry = oracle.mx_unpack(want, mxq.FMT_MX9, 1, cols, "f32", axis=1)
+            assert_bytes_equal(y[r].cpu().view(torch.int32).numpy().view(np.uint8),
+                               ry.view(np.uint8), f"row {r} unpack")
+    else:
+        bpl = rows // 16
+        for c in (0, cols // 2, cols - 1):
+            xc = np.ascontiguousarray(x[:, c:c + 1].cpu().numpy())
+            want = oracle.mx_pack(xc, mxq.FMT_MX9, axis=0)
+            assert_bytes_equal(rec[c * bpl:(c + 1) * bpl].cpu().numpy(), want, f"column {c} records")
+            ry = oracle.mx_unpack(want, mxq.FMT_MX9, rows, 1, "f32", axis=0)
+            got = np.ascontiguousarray(y[:, c:c + 1].cpu().numpy())
+            assert_bytes_equal(got.view(np.uint8), ry.view(np.uint8), f"column {c} unpack")
