@@ -310,3 +310,28 @@ def test_layout_pin_against_cublas_block_scaled_gemm():
             got = _scaled_mm(dev(qa), dev(sa), dev(qb), dev(sb)).cpu().double().numpy()
             _close(got, _dequant(qa, sa, N1, Gk), _dequant(qb, sb, N2, Gk))
         lo = hi
+
+
+def test_two_streams_at_once():
+    """Two casts (and an MX9 pack) in flight on two streams at the same time each
+    give the oracle's bytes: the calls share no scratch state."""
+    xa, oa = W.moe_grouped(M=4096, N=1024, experts=8, routed_units=24, seed=41)
+    xb = W.dual_specials(2048, 2048, seed=42)
+    xm = W.mx9_outliers(1024, 1024, seed=43)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    da, db, dm = to_dev_bf16(xa), to_dev_bf16(xb), torch.from_numpy(xm).cuda()
+    offs = torch.from_numpy(oa).cuda()
+    torch.cuda.synchronize()
+    outs_a, outs_b = dual_outputs(4096, 1024, FILL), dual_outputs(2048, 2048, FILL)
+    with torch.cuda.stream(sa):
+        mxq.quantize_2d_dual(da, offs, out=outs_a, stream=sa)
+        q, e, p = mxq.mx9_pack(dm, stream=sa)
+    with torch.cuda.stream(sb):
+        mxq.quantize_2d_dual(db, None, out=outs_b, stream=sb)
+    torch.cuda.synchronize()
+    for got, x, o, tag in ((outs_a, xa, oa, "stream a "), (outs_b, xb, None, "stream b ")):
+        want = oracle.mxfp8_dual(x, o)
+        assert_dual_equal({k: getattr(got, k).cpu().numpy().reshape(-1) for k in got._fields}, want, tag)
+    rq, re, rp = oracle.mx9_pack(xm)
+    assert_bytes_equal(q.cpu().numpy().view(np.uint8), rq.view(np.uint8), "mx9 q on stream a")
+    assert_bytes_equal(e.cpu().numpy(), re, "mx9 max_exp on stream a")
