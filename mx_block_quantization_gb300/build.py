@@ -23,7 +23,7 @@ BUILD_DIR = PKG / "_build"
 LIB_PATH = PKG / "libmxq.so"
 STAMP = BUILD_DIR / "libmxq.stamp"
 
-SOURCES = ["mxq_dual.cu", "mxq_compose.cu", "mx9.cu", "mx_packed.cu", "mxq_abi.cpp"]
+SOURCES = ["mxq_dual.cu", "mxq_compose.cu", "mx9.cu", "mx_packed.cu", "mx_cols_tma.cu", "mxq_abi.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-diag-suppress", "177", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -18,8 +18,11 @@
 //   its record form; unpacking through mx_unpack_records_kernel, where a warp
 //   copies runs of records into shared memory with 16-byte loads and each lane
 //   then writes 16 output bytes;
-// * blocks along columns: the column-tile kernels, a shared-memory transpose
-//   (vector tiles where rows move in 16-byte pieces, element tiles otherwise);
+// * blocks along columns: where TMA can move the tiles (16-byte aligned x
+//   and packed, row pitch and each column's records multiples of 16 bytes),
+//   the persistent TMA transpose of mx_cols_tma.cu; otherwise the column-tile
+//   kernels here, a shared-memory transpose (vector tiles where rows move in
+//   16-byte pieces, element tiles otherwise);
 // * any other blocked-row tensor (short strided rows, partial last blocks,
 //   unaligned pointers): the generic row kernels, one thread per block, a
 //   warp's 32 consecutive records staged in shared memory and moved with
@@ -966,6 +969,10 @@ extern "C" int mx_pack_packed(const void* x, int dtype, int64_t rows, int64_t co
                                (rows == 1 ? cols : ld) * esize, packed, stream);
   }
   const Geometry g{rows, cols, ld};
+  if (axis == 0 && cols_tma_ok(x, dtype, fmt, rows, cols, ld, packed, false)) {
+    const int r = cols_tma_pack(x, dtype == MXQ_BF16, fmt, rows, cols, ld, packed, stream);
+    if (r != kColsTmaDeclined) return r;
+  }
   if (axis == 0) {
     const uint8_t* xc = static_cast<const uint8_t*>(x);
     const bool pa = aligned_to(packed, 16);
@@ -1016,6 +1023,10 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
                : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb);
   }
   const Geometry g{rows, cols, ld};
+  if (axis == 0 && cols_tma_ok(y, dtype, fmt, rows, cols, ld, packed, true)) {
+    const int r = cols_tma_unpack(packed, fmt, y, dtype == MXQ_BF16, rows, cols, ld, stream);
+    if (r != kColsTmaDeclined) return r;
+  }
   if (axis == 0) {
     const bool pa = aligned_to(packed, 16);
     if (cols_vec_ok(y, dtype, cols, ld)) {

@@ -690,6 +690,7 @@ extern "C" int mxq_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream)
 namespace mxq {
 int mx9_status_read(unsigned int* out, bool clear);      // mx9.cu
 int compose_status_read(unsigned int* out, bool clear);  // mxq_compose.cu
+int cols_status_read(unsigned int* out, bool clear);     // mx_cols_tma.cu
 }
 
 // The device status word is the OR of the per-file words of the kernels.
@@ -706,6 +707,9 @@ extern "C" int mxq_device_status(uint32_t* out, int clear) {
   if (rc != MXQ_OK) return rc;
   rc = mxq::compose_status_read(&c, clear != 0);
   if (rc != MXQ_OK) return rc;
-  *out = v | w | c;
+  unsigned int t = 0;
+  rc = mxq::cols_status_read(&t, clear != 0);
+  if (rc != MXQ_OK) return rc;
+  *out = v | w | c | t;
   return MXQ_OK;
 }

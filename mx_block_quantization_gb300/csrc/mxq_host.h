@@ -58,4 +58,20 @@ inline int sm_count_current_device(int* out_device) {
 int launch_records_pack(const void* x, bool bf16, int fmt, int64_t nb, int64_t nbl, int64_t pitch,
                         uint8_t* packed, cudaStream_t stream);
 
+// The TMA column-tile kernels (mx_cols_tma.cu) for a tensor blocked along its
+// columns: taken when cols_tma_ok accepts the geometry (16-byte aligned x and
+// packed, row pitch a multiple of 16 bytes, each column's records a multiple
+// of 16 bytes, sizes within the int32 tile coordinates; for unpack, writes_x,
+// also rows of a whole number of 16-byte pieces).  The launches return
+// an MXQ_* code, or kColsTmaDeclined when a tensor map cannot be encoded (the
+// caller then takes another kernel).  Arguments already checked.
+constexpr int kColsTmaDeclined = 1;
+bool cols_tma_ok(const void* x, int dtype, int fmt, int64_t rows, int64_t cols, int64_t ld,
+                 const void* packed, bool writes_x);
+int cols_tma_pack(const void* x, bool bf16, int fmt, int64_t rows, int64_t cols, int64_t ld,
+                  uint8_t* packed, cudaStream_t stream);
+int cols_tma_unpack(const uint8_t* packed, int fmt, void* y, bool bf16, int64_t rows, int64_t cols,
+                    int64_t ld, cudaStream_t stream);
+int cols_status_read(unsigned int* out, bool clear);
+
 }  // namespace mxq

@@ -66,6 +66,32 @@ def test_packed_shapes(fmt, dt, axis, rows, cols, ld):
     _check(x, cols, fmt, axis, f"fmt{fmt} {dt} axis{axis} {rows}x{cols}/{ld}")
 
 
+def _tma_cols_geometry(fmt: int, dt: str, rows: int, ld: int) -> bool:
+    """Blocks along columns move as TMA tiles when the row pitch and each
+    column's records are multiples of 16 bytes (pointers here are aligned)."""
+    rec = 18 if fmt == mxq.FMT_MX9 else 12
+    return (ld * (2 if dt == "bf16" else 4)) % 16 == 0 and (-(-rows // 16) * rec) % 16 == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols,ld", [(120, 37, 40), (120, 38, 40), (248, 36, 40),
+                                          (128, 300, 304), (113, 8, 8), (1020, 700, 704),
+                                          (2048, 1000, 1000), (4096, 4096, 4096), (60, 1, 8),
+                                          (250, 129, 136), (3968, 2304, 2312)])
+def test_packed_cols_tma_tiles(fmt, dt, rows, cols, ld):
+    """Blocks along columns through the TMA tiles: ragged columns and rows
+    (partial tiles and blocks), padded pitches, several tiles per CTA."""
+    if not _tma_cols_geometry(fmt, dt, rows, ld):
+        pytest.skip("geometry outside the TMA tiles for this format")
+    x = np.zeros((rows, ld), np.float32)
+    x[:, :cols] = W.mx9_outliers(rows, cols, seed=rows + 7 * cols, zero_blocks=0, tiny_blocks=0)
+    x[:, cols:] = np.float32(-7e33)                  # outside the tensor: must not matter
+    if dt == "bf16":
+        x = W.f32_to_bf16_bits(x)
+    _check(x, cols, fmt, 0, f"fmt{fmt} {dt} axis0 {rows}x{cols}/{ld}")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("axis", [0, 1])
 def test_packed_outlier_workload(fmt, axis):
