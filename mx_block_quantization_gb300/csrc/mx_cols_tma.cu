@@ -191,6 +191,8 @@ struct LaneGeo {
   }
 };
 
+// mbarriers after the data: full / empty per ring stage, and out-full /
+// out-free per staged record buffer (pack only), then the CTA's abort flag.
 struct Barriers {
   uint32_t base;
   int stages;
