@@ -183,3 +183,70 @@ def test_packed_calls_replay_in_a_cuda_graph(fmt, axis, pitch):
     torch.cuda.synchronize()
     assert torch.equal(rec, rec_eager)
     assert torch.equal(y.contiguous().view(torch.int32), y_eager.contiguous().view(torch.int32))
+
+
+def _fuzz_case(i: int):
+    """Seeded geometry i.  Odd-numbered quarters of the cases are aligned (16-byte
+    element and record offsets and pitches, whole 16-element blocks or sizes
+    just under a tile) so that the vector, record and TMA kernels are reached;
+    the others take arbitrary sizes, pitches and offsets."""
+    g = np.random.Generator(np.random.PCG64(1000 + i))
+    dt = ("f32", "bf16")[i % 2]
+    fmt = FMTS[(i // 2) % 2]
+    axis = (i // 4) % 2
+    es = 4 if dt == "f32" else 2
+    if (i // 8) % 2:  # aligned
+        unit = 16 // es  # elements per 16 bytes
+        run = 128 if fmt == mxq.FMT_MX9 else 64  # rows whose records fill 16-byte runs
+        rows = int(run * g.integers(1, 5) - g.integers(0, 16))
+        cols = int(16 * g.integers(1, 40)) if g.random() < 0.5 else int(unit * g.integers(1, 90))
+        pad = int(unit * g.choice([0, 0, 1, 2, 5]))
+        x_off = int(unit * g.choice([0, 1]))
+        p_off = int(g.choice([0, 8]))  # 0 or 16 / 32 bytes
+    else:
+        rows = int(g.integers(1, 400))
+        cols = int(g.integers(1, 700))
+        pad = int(g.choice([0, 0, 1, 3, 4, 8, 16, 37]))
+        x_off = int(g.choice([0, 0, 1, 4, 8]))
+        p_off = int(g.choice([0, 0, 1, 8]))  # in units of the record alignment (2 or 4 bytes)
+    return dt, fmt, axis, rows, cols, pad, x_off, p_off
+
+
+@pytest.mark.parametrize("i", range(64))
+def test_packed_random_geometries(i):
+    """64 seeded geometries through whichever kernel each one selects (TMA
+    column tiles, vector or element column tiles, record rows, generic rows):
+    records and the unpacked tensor equal the oracle, and nothing outside the
+    tensor's elements (pitch padding, the bytes before an offset view) changes."""
+    dt, fmt, axis, rows, cols, pad, x_off, p_off = _fuzz_case(i)
+    is_bf16 = dt == "bf16"
+    pitch = cols + pad
+    xs = W.mx9_outliers(rows, cols, seed=i, zero_blocks=0, tiny_blocks=0)
+    full = np.full((rows, pitch), np.float32(-6e35), np.float32)
+    full[:, :cols] = xs
+    if is_bf16:
+        full = W.f32_to_bf16_bits(full)
+    want = oracle.mx_pack(full, fmt, axis=axis, cols=cols)
+    flat = np.concatenate([np.zeros(x_off, full.dtype), full.reshape(-1)])
+    xd = _dev(flat)[x_off:].view(rows, pitch)[:, :cols]
+    rb = mxq.RECORD_BYTES[fmt]
+    nb = want.shape[0]
+    poff = (2 if fmt == mxq.FMT_MX9 else 4) * p_off
+    big = torch.full((nb * rb + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    pk = big[poff:poff + nb * rb]
+    tag = f"case {i}: {dt} fmt{fmt} axis{axis} {rows}x{cols} pitch {pitch} x_off {x_off} p_off {poff}"
+    mxq.mx_pack_packed(xd, fmt, axis, out=pk)
+    torch.cuda.synchronize()
+    bcpu = big.cpu().numpy()
+    assert_bytes_equal(bcpu[poff:poff + nb * rb].reshape(nb, rb), want, tag + " pack")
+    assert (bcpu[:poff] == 0xAB).all() and (bcpu[poff + nb * rb:] == 0xAB).all(), tag + " outside records"
+    fill = np.full(x_off + rows * pitch, 0x5A5A if is_bf16 else np.float32(-3.25), full.dtype)
+    yflat = _dev(fill)
+    yd = yflat[x_off:].view(rows, pitch)[:, :cols]
+    mxq.mx_unpack_packed(pk, fmt, yd, axis)
+    ref = oracle.mx_unpack(want, fmt, rows, cols, "bf16" if is_bf16 else "f32", axis=axis,
+                           ld=pitch, fill=fill[x_off:].reshape(rows, pitch))
+    torch.cuda.synchronize()
+    got = yflat.cpu().view(torch.int16 if is_bf16 else torch.int32).numpy()
+    assert_bytes_equal(got[x_off:].view(np.uint8), ref.view(np.uint8), tag + " unpack")
+    assert np.array_equal(got[:x_off], fill[:x_off].view(got.dtype)), tag + " before the view"
