@@ -335,3 +335,33 @@ def test_two_streams_at_once():
     rq, re, rp = oracle.mx9_pack(xm)
     assert_bytes_equal(q.cpu().numpy().view(np.uint8), rq.view(np.uint8), "mx9 q on stream a")
     assert_bytes_equal(e.cpu().numpy(), re, "mx9 max_exp on stream a")
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_random_shapes_and_groups(i):
+    """32 seeded configurations: M and N multiples of 128 up to 2560 (tile counts
+    on both sides of the SM count), dense or 1-12 groups with empty groups,
+    leading empty groups and uncovered tails; values from per-band scales with
+    zero, subnormal and non-finite blocks in some cases."""
+    g = np.random.Generator(np.random.PCG64(2000 + i))
+    M = 128 * int(g.integers(1, 21))
+    N = 128 * int(g.integers(1, 21))
+    if g.random() < 0.25:
+        offs = None
+    else:
+        G = int(g.integers(1, 13))
+        cuts = np.sort(g.integers(0, M // 128 + 1, size=G)) * 128
+        if g.random() < 0.5:
+            cuts[-1] = M  # no tail
+        offs = [int(c) for c in cuts]
+    x = W.normal_bf16((M, N), seed=3000 + i, scale=float(2.0 ** g.integers(-20, 20)))
+    if i % 4 == 3:  # specials: a zero block row, subnormals, +-Inf and NaN
+        x = x.copy()
+        x[:32, :] = 0
+        r = g.integers(0, M, size=8)
+        c = g.integers(0, N, size=8)
+        x[r[:2], c[:2]] = 0x7F80          # +Inf
+        x[r[2:4], c[2:4]] = 0xFF80        # -Inf
+        x[r[4:6], c[4:6]] = 0x7FC1        # NaN
+        x[r[6:], c[6:]] = 0x0001          # smallest subnormal
+    _check(x, offs, tag=f"case {i}: {M}x{N} offs {offs} ")

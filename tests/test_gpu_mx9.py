@@ -165,3 +165,18 @@ def test_unpack_with_unaligned_exponent_and_prime_pointers(rows, cols, dt):
         torch.cuda.synchronize()
         got = y.cpu().view(torch.int32 if name == "f32" else torch.int16).numpy()
         assert_bytes_equal(got.view(np.uint8), ry.view(np.uint8), f"unaligned unpack {name}")
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_shapes(i):
+    """16 seeded shapes (1-600 rows, 16-2400 columns in whole blocks), fp32 and
+    bf16, outlier data with zero and ~1e-40 blocks, through the split pack and
+    unpack."""
+    g = np.random.Generator(np.random.PCG64(4000 + i))
+    rows = int(g.integers(1, 601))
+    cols = 16 * int(g.integers(1, 151))
+    nz = min(16, rows * cols // 16 // 8)  # zero and ~1e-40 blocks, as many as fit
+    x = W.mx9_outliers(rows, cols, seed=5000 + i, zero_blocks=nz, tiny_blocks=nz)
+    if i % 2:
+        x = W.f32_to_bf16_bits(x)
+    _check_pack_unpack(x, tag=f"case {i}: {rows}x{cols} {'bf16' if i % 2 else 'f32'} ")
