@@ -279,8 +279,10 @@ constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight p
 // records at a time: copies them into shared memory with 16-byte loads (all
 // loads issued before the first shared store), then each lane rebuilds 16
 // output bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp
-// cover 512 contiguous bytes.  packed and y are 16-byte aligned.
-template <bool kBF16, int kFmt>
+// cover 512 contiguous bytes.  packed and y are 16-byte aligned.  kFlat: the
+// rows follow each other (ld == 16 nbl); a separate instantiation so that
+// the strided form's row bases cost the flat one no registers.
+template <bool kBF16, int kFmt, bool kFlat>
 __global__ void __launch_bounds__(kThreads)
     mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
                              int64_t ld, uint8_t* __restrict__ y) {
@@ -288,13 +290,14 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int kElems = kBF16 ? 8 : 4;  // elements per 16 output bytes
   constexpr int kParts = 16 / kElems;    // output units per block
   constexpr int kGroup = 32 * kRecRuns;  // records per warp iteration
+  constexpr int64_t kEsize = kBF16 ? 2 : 4;
   constexpr int kLoads = (kGroup * RB / 16 + 31) / 32;  // 16-byte loads per lane
   __shared__ __align__(16) uint8_t stage[kWarps][kGroup * kMaxRecord];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t st = smem_u32(stage[warp]);
   const int64_t ngroups = (nb + kGroup - 1) / kGroup;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kWarps;
-  const bool flat = ld == nbl * 16;  // else rows of nbl >= kGroup blocks, ld elements apart
+  constexpr bool flat = kFlat;  // else rows of nbl >= kGroup blocks, ld elements apart
   for (int64_t grp = static_cast<int64_t>(blockIdx.x) * kWarps + warp; grp < ngroups;
        grp += wstride) {
     const int64_t r0 = grp * kGroup;
@@ -319,6 +322,12 @@ __global__ void __launch_bounds__(kThreads)
       asm volatile("st.shared.u16 [%0], %1;" ::"r"(st + 2u * i), "r"(h) : "memory");
     }
     __syncwarp();
+    // strided rows: record r of the group lands at out0 + 16 r elements while
+    // r < split (the rest of row0), at out1 + 16 r past it (the next row; a
+    // group spans at most two rows)
+    const int split = static_cast<int>(nbl - j0 < kGroup ? nbl - j0 : kGroup);
+    uint8_t* const out0 = y + (row0 * ld + j0 * 16) * kEsize;
+    uint8_t* const out1 = y + ((row0 + 1) * ld - (nbl - j0) * 16) * kEsize;
 #pragma unroll
     for (int j = 0; j < kParts * kRecRuns; ++j) {
       const int u = j * 32 + lane;  // output unit of this group
@@ -360,18 +369,12 @@ __global__ void __launch_bounds__(kThreads)
                                           : static_cast<int>(code[k] << 27) >> 27;
         val[k] = fmul_rn_noftz(small_int_float(q), sc);
       }
-      int64_t elem;  // first output element of this 16-byte unit
-      if (flat) {
-        elem = (r0 + r) * 16 + part * kElems;
-      } else {  // a group spans at most two rows
-        int64_t jr = j0 + r, rr = row0;
-        if (jr >= nbl) {
-          jr -= nbl;
-          ++rr;
-        }
-        elem = rr * ld + jr * 16 + part * kElems;
-      }
-      uint8_t* dst = y + elem * (kBF16 ? 2 : 4);
+      // this 16-byte output unit (strided rows: from the group's two row bases,
+      // measured +2 to +13% over per-unit row arithmetic; contiguous rows keep
+      // the flat index, which measured 1-2% faster than the bases there)
+      uint8_t* const dst =
+          flat ? y + ((r0 + r) * 16 + part * kElems) * kEsize
+               : (r < split ? out0 : out1) + static_cast<uint32_t>(r * 16 + part * kElems) * kEsize;
       if (kBF16) {
         uint32_t o[4];
 #pragma unroll
@@ -1014,13 +1017,20 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   uint8_t* yb = static_cast<uint8_t*>(y);
   if (rows_ok(y, dtype, rows, cols, ld, axis, 32 * kRecRuns) && aligned_to(packed, 16)) {
     const int64_t nbl = cols / 16, pitch = rows == 1 ? cols : ld;
+    const int64_t items = (nb + kRecRuns - 1) / kRecRuns;
+    auto go = [&](auto flat_kernel, auto strided_kernel) {
+      return pitch == cols ? launch(flat_kernel, items, stream, packed, nb, nbl, pitch, yb)
+                           : launch(strided_kernel, items, stream, packed, nb, nbl, pitch, yb);
+    };
     if (dtype == MXQ_F32)
-      return fmt == MXQ_FMT_MX9
-                 ? launch(mx_unpack_records_kernel<false, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb)
-                 : launch(mx_unpack_records_kernel<false, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb);
-    return fmt == MXQ_FMT_MX9
-               ? launch(mx_unpack_records_kernel<true, MXQ_FMT_MX9>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb)
-               : launch(mx_unpack_records_kernel<true, MXQ_FMT_MX6>, (nb + kRecRuns - 1) / kRecRuns, stream, packed, nb, nbl, pitch, yb);
+      return fmt == MXQ_FMT_MX9 ? go(mx_unpack_records_kernel<false, MXQ_FMT_MX9, true>,
+                                     mx_unpack_records_kernel<false, MXQ_FMT_MX9, false>)
+                                : go(mx_unpack_records_kernel<false, MXQ_FMT_MX6, true>,
+                                     mx_unpack_records_kernel<false, MXQ_FMT_MX6, false>);
+    return fmt == MXQ_FMT_MX9 ? go(mx_unpack_records_kernel<true, MXQ_FMT_MX9, true>,
+                                   mx_unpack_records_kernel<true, MXQ_FMT_MX9, false>)
+                              : go(mx_unpack_records_kernel<true, MXQ_FMT_MX6, true>,
+                                   mx_unpack_records_kernel<true, MXQ_FMT_MX6, false>);
   }
   const Geometry g{rows, cols, ld};
   if (axis == 0 && cols_tma_ok(y, dtype, fmt, rows, cols, ld, packed, true)) {
