@@ -16,6 +16,10 @@ package imports nothing from the product.
 
 This module only marshals numpy arrays into the C functions; every step of
 the arithmetic is in the C file.
+
+Parity unpinned (not printed on the pages): the bit order of the MX9 / MX6
+prime byte, the sign of the E4M3 NaN byte and the MX6 5-bit code layout.
+Every other result has at least one pin outside the oracle.
 """
 from __future__ import annotations
 

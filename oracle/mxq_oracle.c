@@ -20,6 +20,14 @@
  *
  * Readings where the pages are silent are marked READING and listed in the
  * design notes of the repository.
+ *
+ * Parity unpinned (the pages print none of these, so no pin outside this file
+ * can fix them; the GPU library follows the same readings):
+ *   - the bit order of the MX9 / MX6 prime byte (bit p = pair p, LSB first);
+ *   - the sign of the E4M3 NaN data byte (0x7F);
+ *   - the MX6 code layout (sixteen 5-bit two's-complement codes, element i at
+ *     bits 5i..5i+4 of the 10 data bytes read little-endian).
+ * Every other result here has at least one pin outside this file.
  */
 #include <fenv.h>
 #include <math.h>
