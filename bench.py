@@ -623,9 +623,10 @@ def run_case(args):
     elif args.case.startswith("rec_"):
         # the single packed tensor of MX9 (--fmt 9) or MX6 (--fmt 6) records, rows blocked
         tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
-        xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
+        wide = torch.from_numpy(W.normal_f32((M, N + args.pad), seed=0)).to(dev).to(tdt)
+        xm = wide[:, :N]                       # rows args.pad elements longer than the tensor
         rec = mxq.mx_pack_packed(xm, args.fmt, args.axis)
-        y = torch.empty_like(xm)
+        y = torch.empty_like(wide)[:, :N]
         for _ in range(args.warmup):
             if args.case.startswith("rec_pack"):
                 mxq.mx_pack_packed(xm, args.fmt, args.axis, out=rec)
@@ -643,7 +644,7 @@ def run_case(args):
     torch.cuda.synchronize()
     assert mxq.device_status(clear=True) == 0
     print(json.dumps({"case": args.case, "shape": [M, N], "launches": args.warmup,
-                      **({"fmt": args.fmt, "axis": args.axis} if args.case.startswith("rec_") else {})}))
+                      **({"fmt": args.fmt, "axis": args.axis, "pad": args.pad} if args.case.startswith("rec_") else {})}))
     return 0
 
 
@@ -667,6 +668,8 @@ def main(argv=None):
                     help="with --case rec_*: MX9 or MX6 records")
     ap.add_argument("--axis", type=int, choices=[0, 1], default=1,
                     help="with --case rec_*: blocks along columns (0) or rows (1)")
+    ap.add_argument("--pad", type=int, default=0,
+                    help="with --case rec_*: row pitch = columns + PAD elements")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --case dual: that many K-groups and a 1/8 uncovered tail")
     args = ap.parse_args(argv)
