@@ -259,6 +259,12 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
   return v;
 }
 
+__device__ __forceinline__ float fadd_rn_noftz(float a, float b) {
+  float r;
+  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 // Exact float of a small integer q (|q| < 2^22) without a conversion
 // instruction: the bits of 1.5 * 2^23 + q, minus 1.5 * 2^23.
 __device__ __forceinline__ float small_int_float(int32_t q) {
@@ -358,16 +364,33 @@ __global__ void __launch_bounds__(kThreads)
       const int eb8 = static_cast<int>(head & 0xFFu);
       const uint32_t bits = head >> 8;
       float val[kElems];
+      // the two scales 2^k of the record, k = max(E - off - t, -126): exponent
+      // fields max(eb8 - off - t, 1); one select per element by its pair's bit
+      // (MX9 bf16: +1.5% contiguous, +7.8% strided over per-element scales and
+      // sign extension; fp32 and MX6 within 0.3%)
+      const float s_keep = __uint_as_float(static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset, 1)) << 23);
+      const float s_dem = __uint_as_float(static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset - 1, 1)) << 23);
+      const uint32_t ubits = bits >> (part * kElems / 2);  // this unit's pairs from bit 0
+      if (kFmt == MXQ_FMT_MX9) {
+        // bytes biased by 0x80 under the exponent of 2^23: 2^23 + 128 + q, one
+        // exact subtraction leaves q
 #pragma unroll
-      for (int k = 0; k < kElems; ++k) {
-        const int pair = (part * kElems + k) >> 1;
-        const int t = static_cast<int>((bits >> pair) & 1u);
-        // 2^k, k = max(E - off - t, -126): exponent field max(eb8 - off - t, 1)
-        const float sc = __uint_as_float(
-            static_cast<uint32_t>(max(eb8 - Fmt<kFmt>::kOffset - t, 1)) << 23);
-        const int q = kFmt == MXQ_FMT_MX9 ? static_cast<int>(static_cast<int8_t>(code[k]))
-                                          : static_cast<int>(code[k] << 27) >> 27;
-        val[k] = fmul_rn_noftz(small_int_float(q), sc);
+        for (int k = 0; k < kElems / 4; ++k) {
+          const uint32_t w = __byte_perm(code[4 * k] | (code[4 * k + 1] << 8),
+                                         code[4 * k + 2] | (code[4 * k + 3] << 8), 0x5410) ^ 0x80808080u;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int e = 4 * k + b;
+            const float qf = fadd_rn_noftz(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650 + b)),
+                                           -8388736.0f);
+            val[e] = fmul_rn_noftz(qf, (ubits >> (e >> 1)) & 1u ? s_dem : s_keep);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kElems; ++k)
+          val[k] = fmul_rn_noftz(small_int_float(static_cast<int>(code[k] << 27) >> 27),
+                                 (ubits >> (k >> 1)) & 1u ? s_dem : s_keep);
       }
       // this 16-byte output unit (strided rows: from the group's two row bases,
       // measured +2 to +13% over per-unit row arithmetic; contiguous rows keep
