@@ -58,6 +58,7 @@ typedef struct CUstream_st *cudaStream_t;
 /* ---- device status word bits (see mxq_device_status) ------------------- */
 #define MXQ_DEV_BADOFFS 0x1u /* offs failed the device-side check: no output written */
 #define MXQ_DEV_TIMEOUT 0x2u /* an internal pipeline wait gave up: outputs incomplete */
+#define MXQ_DEV_OOB 0x4u     /* checked build only: a store out of its buffer was skipped */
 
 /*
  * Dual-axis MXFP8 quantization of one bf16 matrix, reading it once.
@@ -272,6 +273,22 @@ int mxq_device_status(uint32_t *out, int clear);
  * usable.  The production kernels use a 4 s limit per wait.
  */
 int mxq_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+/*
+ * Checked builds.  A library compiled with MXQ_DEBUG_BOUNDS=1 (the
+ * package's build step makes it as libmxq_checked.so beside libmxq.so)
+ * tests the byte range of every global store its kernels make outside the
+ * TMA tensor stores (whose bounds the tensor maps enforce) against the
+ * output buffer it belongs to; a range that would leave the buffer is not
+ * written and MXQ_DEV_OOB is set in the device status word.  Results are
+ * otherwise identical.  mxq_debug_bounds() returns 1 in a checked build and
+ * 0 in a release build.  mxq_selftest_bounds() launches one thread that
+ * tests a range lying past a 64-byte dummy buffer, without any access: a
+ * checked build records MXQ_DEV_OOB, a release build records nothing.
+ * Returns MXQ_OK or MXQ_ECUDA.
+ */
+int mxq_debug_bounds(void);
+int mxq_selftest_bounds(cudaStream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *mxq_status_string(int status);

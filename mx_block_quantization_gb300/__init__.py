@@ -19,11 +19,13 @@ Operations (sources by page title):
 from __future__ import annotations
 
 import ctypes
+import os
 from pathlib import Path
 from typing import NamedTuple, Optional
 
 _PKG = Path(__file__).resolve().parent
 LIB_PATH = _PKG / "libmxq.so"
+CHECKED_LIB_PATH = _PKG / "libmxq_checked.so"
 
 # status codes and constants of mxq.h
 OK = 0
@@ -42,6 +44,7 @@ FMT_MX6 = 6
 RECORD_BYTES = {FMT_MX9: 18, FMT_MX6: 12}
 DEV_BADOFFS = 0x1
 DEV_TIMEOUT = 0x2
+DEV_OOB = 0x4  # checked library only: an out-of-buffer access was skipped
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -55,14 +58,18 @@ class MxqError(RuntimeError):
 
 
 def lib() -> ctypes.CDLL:
-    """Load libmxq.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    """Load libmxq.so (built by ``__graft_entry__.build()``); raise if it is missing.
+    With MXQ_CHECKED=1 in the environment, load the bounds-checked twin
+    libmxq_checked.so instead (same results; out-of-buffer accesses skipped and
+    reported as MXQ_DEV_OOB in the device status word)."""
     global _lib
     if _lib is None:
-        if not LIB_PATH.exists():
+        path = CHECKED_LIB_PATH if os.environ.get("MXQ_CHECKED") == "1" else LIB_PATH
+        if not path.exists():
             raise ImportError(
-                f"{LIB_PATH.name} is not built; run `python -c 'import __graft_entry__ as g; "
+                f"{path.name} is not built; run `python -c 'import __graft_entry__ as g; "
                 f"g.build()'` (there is no CPU fallback)")
-        L = ctypes.CDLL(str(LIB_PATH))
+        L = ctypes.CDLL(str(path))
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
         L.mxq_quantize_2d_dual.restype = ctypes.c_int
         L.mxq_quantize_2d_dual.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
@@ -88,6 +95,10 @@ def lib() -> ctypes.CDLL:
                                        ctypes.c_int, vp]
         L.mxq_selftest_wait_timeout.restype = ctypes.c_int
         L.mxq_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.mxq_debug_bounds.restype = ctypes.c_int
+        L.mxq_debug_bounds.argtypes = []
+        L.mxq_selftest_bounds.restype = ctypes.c_int
+        L.mxq_selftest_bounds.argtypes = [vp]
         L.mxq_device_status.restype = ctypes.c_int
         L.mxq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.mxq_status_string.restype = ctypes.c_char_p
@@ -124,6 +135,21 @@ def selftest_wait_timeout(limit_ns: int = 50_000_000, stream=None) -> None:
     rc = lib().mxq_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(s.cuda_stream))
     if rc != OK:
         raise MxqError(rc, "mxq_selftest_wait_timeout")
+
+
+def debug_bounds() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().mxq_debug_bounds())
+
+
+def selftest_bounds(stream=None) -> None:
+    """Launch the bounds-check self-test (see mxq.h); afterwards device_status()
+    reports DEV_OOB in the checked library and nothing in the release one."""
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = lib().mxq_selftest_bounds(ctypes.c_void_p(s.cuda_stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_selftest_bounds")
 
 
 # ---------------------------------------------------------------------------

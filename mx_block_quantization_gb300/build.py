@@ -22,6 +22,10 @@ INCLUDE = ROOT / "include"
 BUILD_DIR = PKG / "_build"
 LIB_PATH = PKG / "libmxq.so"
 STAMP = BUILD_DIR / "libmxq.stamp"
+# the checked build: every computed global access tested against its buffer
+# (MXQ_DEBUG_BOUNDS=1, see csrc/mxq_check.cuh); same kernels otherwise
+CHECKED_LIB_PATH = PKG / "libmxq_checked.so"
+CHECKED_FLAGS = ["-DMXQ_DEBUG_BOUNDS=1"]
 
 SOURCES = ["mxq_dual.cu", "mxq_compose.cu", "mx9.cu", "mx_packed.cu", "mx_cols_tma.cu", "mxq_abi.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -36,27 +40,32 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _fingerprint() -> str:
+def _fingerprint(extra=()) -> str:
     h = hashlib.sha256()
     for f in sorted(list(CSRC.glob("*")) + list(INCLUDE.glob("*.h"))):
         if f.is_file():
             h.update(f.name.encode())
             h.update(f.read_bytes())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    h.update(" ".join(ARCH + NVCC_FLAGS + list(extra)).encode())
     h.update(platform.machine().encode())
     return h.hexdigest()
 
 
-def build_library(force: bool = False, verbose: bool = False) -> Path:
-    fp = _fingerprint()
-    if not force and LIB_PATH.exists() and STAMP.exists() and STAMP.read_text() == fp:
-        return LIB_PATH
-    BUILD_DIR.mkdir(exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, checked: bool = False) -> Path:
+    """Build libmxq.so, or with `checked` the bounds-checked libmxq_checked.so."""
+    extra = CHECKED_FLAGS if checked else []
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    build_dir = BUILD_DIR / "checked" if checked else BUILD_DIR
+    stamp = build_dir / (lib_path.stem + ".stamp")
+    fp = _fingerprint(extra)
+    if not force and lib_path.exists() and stamp.exists() and stamp.read_text() == fp:
+        return lib_path
+    build_dir.mkdir(parents=True, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src: str) -> Path:
-        obj = BUILD_DIR / (src + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", str(CSRC / src), "-o", str(obj)]
+        obj = build_dir / (src + ".o")
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", str(CSRC / src), "-o", str(obj)]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.run(cmd, check=True)
@@ -64,13 +73,13 @@ def build_library(force: bool = False, verbose: bool = False) -> Path:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH.with_name(f".libmxq.{os.getpid()}.so")
+    tmp = lib_path.with_name(f".libmxq.{os.getpid()}.so")
     subprocess.run([cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *map(str, objs), "-o", str(tmp)],
                    check=True)
-    os.replace(tmp, LIB_PATH)
-    STAMP.write_text(fp)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    stamp.write_text(fp)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build_library(force="--force" in sys.argv, verbose=True))
+    print(build_library(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

@@ -27,6 +27,7 @@
 
 #include "mxq.h"
 #include "mx_block.cuh"
+#include "mxq_check.cuh"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
 
@@ -192,15 +193,23 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
       const uint32_t bytes = static_cast<uint32_t>(nblk) * S::kBlockBytes;
       mbar_arrive_expect_tx(full(s), bytes);
       const uint32_t dst = base + static_cast<uint32_t>(s) * S::kStageBytes;
+      // x: nb / nbl rows of nbl blocks, pitch bytes apart
+      const uint64_t x_bytes = static_cast<uint64_t>(nb / nbl - 1) * pitch + nbl * S::kBlockBytes;
       if (pitch == nbl * static_cast<int64_t>(S::kBlockBytes)) {  // rows follow each other
-        bulk_load_1d(dst, x + b0 * S::kBlockBytes, bytes, full(s));
+        if (in_buf(x + b0 * S::kBlockBytes, bytes, x, x_bytes, &g_mx9_status))
+          bulk_load_1d(dst, x + b0 * S::kBlockBytes, bytes, full(s));
+        else
+          mbar_complete_tx(full(s), bytes);
       } else {  // one copy per row piece of the stage's blocks
         int64_t row = b0 / nbl, j = b0 - row * nbl;
         for (int64_t b = b0; b < b0 + nblk; ++row, j = 0) {
           const int64_t n = b0 + nblk - b < nbl - j ? b0 + nblk - b : nbl - j;
-          bulk_load_1d(dst + static_cast<uint32_t>(b - b0) * S::kBlockBytes,
-                       x + row * pitch + j * S::kBlockBytes,
-                       static_cast<uint32_t>(n) * S::kBlockBytes, full(s));
+          const uint32_t nbytes = static_cast<uint32_t>(n) * S::kBlockBytes;
+          if (in_buf(x + row * pitch + j * S::kBlockBytes, nbytes, x, x_bytes, &g_mx9_status))
+            bulk_load_1d(dst + static_cast<uint32_t>(b - b0) * S::kBlockBytes,
+                         x + row * pitch + j * S::kBlockBytes, nbytes, full(s));
+          else
+            mbar_complete_tx(full(s), nbytes);
           b += n;
         }
       }
@@ -254,9 +263,12 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
         if (blk >= nb) break;
         uint32_t h[8], eb8, bits;
         quantize(local, h, &eb8, &bits);
-        __stcs(reinterpret_cast<uint4*>(q_or_rec) + blk, pairs_to_bytes(h));
-        max_exp[blk] = static_cast<uint8_t>(eb8);
-        prime[blk] = static_cast<uint8_t>(bits);
+        if (in_buf(q_or_rec + 16 * blk, 16, q_or_rec, 16ull * nb, &g_mx9_status))
+          __stcs(reinterpret_cast<uint4*>(q_or_rec) + blk, pairs_to_bytes(h));
+        if (in_buf(max_exp + blk, 1, max_exp, nb, &g_mx9_status))
+          max_exp[blk] = static_cast<uint8_t>(eb8);
+        if (in_buf(prime + blk, 1, prime, nb, &g_mx9_status))
+          prime[blk] = static_cast<uint8_t>(bits);
       }
     } else {
       const int64_t wrun0 = blk0 + static_cast<int64_t>(warp) * S::kWarpBlocks;
@@ -276,7 +288,10 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
         }
         const int64_t nvalid = nb - wrun0 < S::kWarpBlocks ? nb - wrun0 : S::kWarpBlocks;
         const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kRecord;
-        if (bytes % 16u == 0) {
+        if (!in_buf(q_or_rec + wrun0 * S::kRecord, bytes, q_or_rec,
+                    static_cast<uint64_t>(nb) * S::kRecord, &g_mx9_status)) {
+          __syncwarp();
+        } else if (bytes % 16u == 0) {
           fence_proxy_async_smem();  // staged records before the bulk store reads them
           __syncwarp();
           if (lane == 0) {
@@ -364,15 +379,24 @@ __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
     for (int u = 0; u < U::kUnroll; ++u) {
       const int64_t c = base + u * stride + lane;
       if (c < nchunks) {
-        if (kBF16) {
-          const uint2 w = __ldcs(reinterpret_cast<const uint2*>(q) + c);
-          qv[u][0] = w.x;
-          qv[u][U::kElems / 4 - 1] = w.y;
+        // q: nchunks * kElems bytes; exponent and prime bytes: one per block
+        const uint64_t nblk = static_cast<uint64_t>(nchunks) / U::kLanesPerBlock;
+        if (in_buf(reinterpret_cast<const uint8_t*>(q) + U::kElems * c, U::kElems, q,
+                   static_cast<uint64_t>(nchunks) * U::kElems, &g_mx9_status) &&
+            in_buf(max_exp + c / U::kLanesPerBlock, 1, max_exp, nblk, &g_mx9_status) &&
+            in_buf(prime + c / U::kLanesPerBlock, 1, prime, nblk, &g_mx9_status)) {
+          if (kBF16) {
+            const uint2 w = __ldcs(reinterpret_cast<const uint2*>(q) + c);
+            qv[u][0] = w.x;
+            qv[u][U::kElems / 4 - 1] = w.y;
+          } else {
+            qv[u][0] = __ldcs(q + c);
+          }
+          ev[u] = __ldg(max_exp + c / U::kLanesPerBlock);
+          pv[u] = __ldg(prime + c / U::kLanesPerBlock);
         } else {
-          qv[u][0] = __ldcs(q + c);
+          qv[u][0] = qv[u][U::kElems / 4 - 1] = ev[u] = pv[u] = 0;
         }
-        ev[u] = __ldg(max_exp + c / U::kLanesPerBlock);
-        pv[u] = __ldg(prime + c / U::kLanesPerBlock);
       } else {
         qv[u][0] = qv[u][U::kElems / 4 - 1] = ev[u] = pv[u] = 0;
       }
@@ -400,7 +424,9 @@ __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
 #pragma unroll
         for (int k = 0; k < U::kElems / 4; ++k) unpack4(qv[u][k], s[2 * k], s[2 * k + 1], v + 4 * k);
       }
-      if (kBF16) {
+      if (!in_buf(reinterpret_cast<uint8_t*>(y) + 16 * c, 16, y, 16ull * nchunks, &g_mx9_status)) {
+        continue;
+      } else if (kBF16) {
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // the high halves of two fp32 values

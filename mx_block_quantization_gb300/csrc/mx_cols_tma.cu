@@ -44,6 +44,7 @@
 #include <stdint.h>
 
 #include "mx_block.cuh"
+#include "mxq_check.cuh"
 #include "mxq.h"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
@@ -467,7 +468,9 @@ __global__ void __launch_bounds__(kUnpackThreads, 1)
           const uint4 q = lds128(ytile + static_cast<uint32_t>(pbox) * kBoxBytes +
                                  static_cast<uint32_t>(r) * 128u +
                                  (static_cast<uint32_t>(pchunk ^ (r & 7)) << 4));
-          __stcs(reinterpret_cast<uint4*>(p + r * pitch), q);
+          if (in_buf(p + r * pitch, 16, y, static_cast<uint64_t>((rows - 1) * ld + cols) * C::kEsize,
+                     &g_cols_status))
+            __stcs(reinterpret_cast<uint4*>(p + r * pitch), q);
         }
       }
     }

@@ -32,6 +32,7 @@
 
 #include "mx_block.cuh"
 #include "mxq.h"
+#include "mxq_check.cuh"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
 
@@ -54,6 +55,20 @@ struct Fmt {
 struct Geometry {
   int64_t rows, cols, ld;
 };
+
+// Sticky status word of this file's kernels (MXQ_DEV_* bits).
+__device__ unsigned int g_packed_status = 0;
+
+// Bytes from the first to one past the last element of the tensor.
+__device__ __forceinline__ uint64_t span_bytes(const Geometry& g, int esize) {
+  return g.rows > 0 && g.cols > 0 ? static_cast<uint64_t>((g.rows - 1) * g.ld + g.cols) * esize : 0;
+}
+
+// Bytes of the packed tensor of g blocked along rows (axis 1) or columns.
+__device__ __forceinline__ uint64_t packed_bytes(const Geometry& g, bool along_rows, int rb) {
+  const int64_t lines = along_rows ? g.rows : g.cols, len = along_rows ? g.cols : g.rows;
+  return static_cast<uint64_t>(lines * ((len + 15) / 16)) * rb;
+}
 
 template <bool kBF16>
 __device__ __forceinline__ uint32_t load_bits(const uint8_t* x, int64_t idx) {
@@ -144,7 +159,11 @@ __global__ void __launch_bounds__(kThreads)
       const int64_t valid = min(static_cast<int64_t>(16), g.cols - 16 * j);
       const int64_t e0 = row * g.ld + 16 * j;  // first element of the block
       uint32_t f[16];
-      if (vec_rows && valid == 16) {
+      constexpr int kEs = kBF16 ? 2 : 4;
+      if (!in_buf(x + e0 * kEs, valid * kEs, x, span_bytes(g, kEs), &g_packed_status)) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = 0u;
+      } else if (vec_rows && valid == 16) {
         const uint8_t* src = x + e0 * (kBF16 ? 2 : 4);
         if (kBF16) {
 #pragma unroll
@@ -178,7 +197,8 @@ __global__ void __launch_bounds__(kThreads)
     // the warp's records w0 .. w0+31 are contiguous
     __syncwarp();
     const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
-    warp_copy_out(packed + w0 * RB, stage[warp], static_cast<int>(nvalid) * RB, packed_aligned, lane);
+    if (in_buf(packed + w0 * RB, nvalid * RB, packed, packed_bytes(g, true, RB), &g_packed_status))
+      warp_copy_out(packed + w0 * RB, stage[warp], static_cast<int>(nvalid) * RB, packed_aligned, lane);
     __syncwarp();
   }
 }
@@ -198,7 +218,8 @@ __global__ void __launch_bounds__(kThreads)
     uint32_t rec[5] = {0, 0, 0, 0, 0};
     uint8_t* st = stage[warp];
     const int64_t nvalid = min(static_cast<int64_t>(32), nb - w0);
-    warp_copy_in(st, packed + w0 * RB, static_cast<int>(nvalid) * RB, packed_aligned, lane);
+    if (in_buf(packed + w0 * RB, nvalid * RB, packed, packed_bytes(g, true, RB), &g_packed_status))
+      warp_copy_in(st, packed + w0 * RB, static_cast<int>(nvalid) * RB, packed_aligned, lane);
     __syncwarp();
     if (w < nb) {
       const uint16_t* h = reinterpret_cast<const uint16_t*>(st + lane * RB);
@@ -223,7 +244,10 @@ __global__ void __launch_bounds__(kThreads)
       v[i] = fmul_rn_noftz(static_cast<float>(q[i]), __uint_as_float(static_cast<uint32_t>(kf) << 23));
     }
     const int64_t valid = min(static_cast<int64_t>(16), g.cols - 16 * j);
-    if (vec_rows && valid == 16) {
+    if (!in_buf(y + e0 * (kBF16 ? 2 : 4), valid * (kBF16 ? 2 : 4), y, span_bytes(g, kBF16 ? 2 : 4),
+                &g_packed_status)) {
+      continue;
+    } else if (vec_rows && valid == 16) {
       uint8_t* dst = y + e0 * (kBF16 ? 2 : 4);
       if (kBF16) {
 #pragma unroll
@@ -311,7 +335,8 @@ __global__ void __launch_bounds__(kThreads)
     const int nvalid = static_cast<int>(nb - r0 < kGroup ? nb - r0 : kGroup);
     // copy in: 16-byte units, then 2-byte pieces
     const uint8_t* src = packed + r0 * RB;
-    const int bytes = nvalid * RB, n16 = bytes >> 4;
+    const int bytes = nvalid * RB;
+    const int n16 = in_buf(src, bytes, packed, static_cast<uint64_t>(nb) * RB, &g_packed_status) ? bytes >> 4 : 0;
     uint4 v[kLoads];
 #pragma unroll
     for (int k = 0; k < kLoads; ++k) {
@@ -323,7 +348,7 @@ __global__ void __launch_bounds__(kThreads)
       const int i = lane + 32 * k;
       if (i < n16) sts128(st + 16u * i, v[k].x, v[k].y, v[k].z, v[k].w);
     }
-    for (int i = n16 * 8 + lane; i < (bytes >> 1); i += 32) {
+    for (int i = n16 * 8 + lane; i < (n16 ? bytes >> 1 : 0); i += 32) {
       const uint32_t h = __ldcs(reinterpret_cast<const uint16_t*>(src) + i);
       asm volatile("st.shared.u16 [%0], %1;" ::"r"(st + 2u * i), "r"(h) : "memory");
     }
@@ -398,7 +423,11 @@ __global__ void __launch_bounds__(kThreads)
       uint8_t* const dst =
           flat ? y + ((r0 + r) * 16 + part * kElems) * kEsize
                : (r < split ? out0 : out1) + static_cast<uint32_t>(r * 16 + part * kElems) * kEsize;
-      if (kBF16) {
+      // y spans (nb / nbl - 1) * ld + 16 nbl elements
+      if (!in_buf(dst, 16, y, static_cast<uint64_t>((nb / nbl - 1) * ld + 16 * nbl) * kEsize,
+                  &g_packed_status)) {
+        continue;
+      } else if (kBF16) {
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -461,7 +490,10 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll 8
     for (int r = warp; r < kColTileRows; r += kWarps) {
       const int64_t row = r0 + r;
-      const uint32_t v = (col_ok && row < g.rows) ? load_bits<kBF16>(x, row * g.ld + c0 + lane) : 0u;
+      const bool ld_ok = col_ok && row < g.rows &&
+                         in_buf(x + (row * g.ld + c0 + lane) * (kBF16 ? 2 : 4), kBF16 ? 2 : 4, x,
+                                span_bytes(g, kBF16 ? 2 : 4), &g_packed_status);
+      const uint32_t v = ld_ok ? load_bits<kBF16>(x, row * g.ld + c0 + lane) : 0u;
       if (kBF16)
         sts16(tile + 2u * col_swizzle(r, lane), v >> 16);
       else
@@ -490,8 +522,9 @@ __global__ void __launch_bounds__(kThreads)
       }
       __syncwarp();
       const int64_t b0 = (c0 + cc) * nbl + tr * 32;
-      warp_copy_out(packed + b0 * RB, stage, nvalid * RB,
-                    packed_aligned && ((b0 * RB) & 15) == 0, lane);
+      if (in_buf(packed + b0 * RB, nvalid * RB, packed, packed_bytes(g, false, RB), &g_packed_status))
+        warp_copy_out(packed + b0 * RB, stage, nvalid * RB,
+                      packed_aligned && ((b0 * RB) & 15) == 0, lane);
       __syncwarp();
     }
     __syncthreads();
@@ -519,7 +552,15 @@ __global__ void __launch_bounds__(kThreads)
     const int nvalid = static_cast<int>(nbl - tr * 32 < 32 ? nbl - tr * 32 : 32);
     // copy in the records of this warp's columns (cc = warp + kWarps * k): with
     // 16-byte loads, all issued before the first shared store, when aligned
-    const int bytes = nvalid * RB;
+    // every run this warp reads lies inside the packed tensor (checked builds)
+    bool runs_ok = true;
+    for (int k = 0; k < T::kColsPerWarp; ++k) {
+      const int64_t col = c0 + warp + kWarps * k;
+      if (col < g.cols)
+        runs_ok &= in_buf(packed + (col * nbl + tr * 32) * RB, nvalid * RB, packed,
+                          packed_bytes(g, false, RB), &g_packed_status);
+    }
+    const int bytes = runs_ok ? nvalid * RB : 0;
     const bool fast = packed_aligned && ((nbl * RB) & 15) == 0 && ((tr * 32 * RB) & 15) == 0;
     if (fast) {
       uint4 v[T::kColsPerWarp][kLoads];
@@ -591,6 +632,9 @@ __global__ void __launch_bounds__(kThreads)
       const int64_t row = r0 + r;
       if (!col_ok || row >= g.rows) continue;
       const int64_t idx = row * g.ld + c0 + lane;
+      if (!in_buf(y + idx * (kBF16 ? 2 : 4), kBF16 ? 2 : 4, y, span_bytes(g, kBF16 ? 2 : 4),
+                  &g_packed_status))
+        continue;
       if (kBF16)
         reinterpret_cast<uint16_t*>(y)[idx] = static_cast<uint16_t>(lds16(tile + 2u * col_swizzle(r, lane)));
       else
@@ -704,10 +748,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int k = 0; k < kVecTileRows / kWarps; ++k) {
       const int r = warp + kWarps * k;
-      const bool in = piece_ok && r0 + r < g.rows;
+      const uint8_t* src = xrow + static_cast<int64_t>(kWarps * k) * g.ld * esize;
+      const bool in = piece_ok && r0 + r < g.rows &&
+                      in_buf(src, 16, x, span_bytes(g, esize), &g_packed_status);
       const uint32_t dst = tile + static_cast<uint32_t>(r) * kVecRowBytes +
                            (static_cast<uint32_t>(lane ^ ((k >> 1) & 7)) << 4);
-      cp_async_16(dst, in ? xrow + static_cast<int64_t>(kWarps * k) * g.ld * esize : x, in ? 16u : 0u);
+      cp_async_16(dst, in ? src : x, in ? 16u : 0u);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -744,7 +790,8 @@ __global__ void __launch_bounds__(kThreads)
       for (int k = 0; k < V::kColsPerStep / 4; ++k) {
         const int ci = cidx + 4 * k;
         const int64_t col = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + ci;
-        if (col < g.cols) {
+        if (col < g.cols && in_buf(packed + (col * nbl + tr * 8) * RB, nvalid * RB, packed,
+                                   packed_bytes(g, false, RB), &g_packed_status)) {
           const int64_t b0 = col * nbl + tr * 8;
           run_copy_out(packed + b0 * RB, stage + ci * 8 * RB, nvalid * RB,
                        packed_aligned && ((b0 * RB) & 15) == 0 && ((ci * 8 * RB) & 15) == 0,
@@ -832,6 +879,9 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t col = c0 + static_cast<int64_t>(pg) * V::kColsPerPiece + ci;
         const uint8_t* src = packed + (col * nbl + tr * 8) * RB;
         uint8_t* dst = slot + ci * kRunBytes;
+        // runs of columns past the tensor are never decoded into its rows
+        if (col >= g.cols || !in_buf(src, bytes, packed, packed_bytes(g, false, RB), &g_packed_status))
+          continue;
         if (async_in) {
           for (int u = lane & 7; u < (kRunBytes + 15) / 16; u += 8) {
             const int left = bytes - 16 * u;
@@ -883,9 +933,11 @@ __global__ void __launch_bounds__(kThreads)
     for (int k = 0; k < kVecTileRows / kWarps; ++k) {
       const int r = warp + kWarps * k;
       if (!piece_ok || r0 + r >= g.rows) continue;
+      uint8_t* const dst = yrow + static_cast<int64_t>(kWarps * k) * g.ld * esize;
+      if (!in_buf(dst, 16, y, span_bytes(g, esize), &g_packed_status)) continue;
       const uint4 v = lds128(tile + static_cast<uint32_t>(r) * kVecRowBytes +
                              (static_cast<uint32_t>(lane ^ ((k >> 1) & 7)) << 4));
-      __stcs(reinterpret_cast<uint4*>(yrow + static_cast<int64_t>(kWarps * k) * g.ld * esize), v);
+      __stcs(reinterpret_cast<uint4*>(dst), v);
     }
     __syncthreads();
   }
@@ -980,6 +1032,12 @@ int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
+}
+
+// One thread tests a byte range that starts at the end of a 64-byte dummy
+// buffer: in a checked build that records MXQ_DEV_OOB; nothing is accessed.
+__global__ void selftest_bounds_kernel(const uint8_t* buf) {
+  (void)in_buf(buf + 64, 16, buf, 64, &g_packed_status);
 }
 
 }  // namespace
@@ -1089,4 +1147,27 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   return fmt == MXQ_FMT_MX9
              ? launch(mx_unpack_packed_kernel<true, MXQ_FMT_MX9>, nb, stream, packed, g, vec_rows, pal, yb)
              : launch(mx_unpack_packed_kernel<true, MXQ_FMT_MX6>, nb, stream, packed, g, vec_rows, pal, yb);
+}
+
+namespace mxq {
+int packed_status_read(unsigned int* out, bool clear) {
+  if (cudaMemcpyFromSymbol(out, g_packed_status, sizeof *out) != cudaSuccess) return MXQ_ECUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_packed_status, &zero, sizeof zero) != cudaSuccess) return MXQ_ECUDA;
+  }
+  return MXQ_OK;
+}
+}  // namespace mxq
+
+extern "C" int mxq_debug_bounds(void) { return MXQ_DEBUG_BOUNDS ? 1 : 0; }
+
+extern "C" int mxq_selftest_bounds(cudaStream_t stream) {
+  // the dummy buffer's address is only compared, never dereferenced
+  const uint8_t* buf = reinterpret_cast<const uint8_t*>(uintptr_t{1} << 20);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, selftest_bounds_kernel, buf) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "mxq.h"
+#include "mxq_check.cuh"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
 
@@ -94,12 +95,15 @@ __global__ void __launch_bounds__(kSwzThreads)
       const int64_t n0 = 128 * (al / A) + k;
       const int64_t col = lo / 32 + 4 * (al % A);
       const uint8_t* src = s_rm + n0 * pitch + col;
-      out.x = __ldg(reinterpret_cast<const uint32_t*>(src));
-      out.y = __ldg(reinterpret_cast<const uint32_t*>(src + 32 * pitch));
-      out.z = __ldg(reinterpret_cast<const uint32_t*>(src + 64 * pitch));
-      out.w = __ldg(reinterpret_cast<const uint32_t*>(src + 96 * pitch));
+      if (in_buf(src, 96 * pitch + 4, s_rm, static_cast<uint64_t>(N) * M / 32, &g_compose_status)) {
+        out.x = __ldg(reinterpret_cast<const uint32_t*>(src));
+        out.y = __ldg(reinterpret_cast<const uint32_t*>(src + 32 * pitch));
+        out.z = __ldg(reinterpret_cast<const uint32_t*>(src + 64 * pitch));
+        out.w = __ldg(reinterpret_cast<const uint32_t*>(src + 96 * pitch));
+      }
     }
-    reinterpret_cast<uint4*>(s_col)[u] = out;
+    if (in_buf(s_col + 16 * u, 16, s_col, static_cast<uint64_t>(N) * M / 32, &g_compose_status))
+      reinterpret_cast<uint4*>(s_col)[u] = out;
   }
 }
 

@@ -29,6 +29,7 @@
 #include <mutex>
 
 #include "mxq.h"
+#include "mxq_check.cuh"
 #include "mxq_device.cuh"
 #include "mxq_host.h"
 
@@ -428,7 +429,9 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
           const int n = lane + 32 * r;
           const uint32_t word =
               lds32(base + kOffSCol + b * kAtomBytes + static_cast<uint32_t>((n & 31) * 16 + (n >> 5) * 4));
-          *reinterpret_cast<uint32_t*>(s_col + (tj * kTile + n) * pitch + 4 * ti) = word;
+          uint8_t* const dst = s_col + (tj * kTile + n) * pitch + 4 * ti;
+          if (in_buf(dst, 4, s_col, static_cast<uint64_t>(N) * Mrows / 32, &g_mxq_status))
+            *reinterpret_cast<uint32_t*>(dst) = word;
         }
         __syncwarp();
       }
@@ -441,8 +444,10 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
           else
             tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
                          base + kOffQRow + b * kQTileBytes);
-          bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
-                     kAtomBytes);
+          if (in_buf(s_row + (ti * TN + tj) * kAtomBytes, kAtomBytes, s_row,
+                     static_cast<uint64_t>(N) * Mrows / 32, &g_mxq_status))
+            bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
+                       kAtomBytes);
         }
         if (R::kCol) {
           if (MXQ_DUAL_L2_HINTS & 2)
@@ -464,11 +469,13 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
             const int64_t atoms_per_nblock = (hi - lo) / kTile;  // (hi-lo)/32 scale cols / 4
             uint8_t* dst = s_col + static_cast<int64_t>(N) * lo / 32 +
                            (tj * atoms_per_nblock + (grow - lo) / kTile) * kAtomBytes;
-            bulk_store(dst, base + kOffSCol + b * kAtomBytes, kAtomBytes);
+            if (in_buf(dst, kAtomBytes, s_col, static_cast<uint64_t>(N) * Mtot / 32, &g_mxq_status))
+              bulk_store(dst, base + kOffSCol + b * kAtomBytes, kAtomBytes);
           } else {
             uint8_t* dst = s_col + static_cast<int64_t>(N) * end_rows / 32 +
                            (((grow - end_rows) / kTile) * TN + tj) * kAtomBytes;
-            bulk_store(dst, base + kOffZero, kAtomBytes);
+            if (in_buf(dst, kAtomBytes, s_col, static_cast<uint64_t>(N) * Mtot / 32, &g_mxq_status))
+              bulk_store(dst, base + kOffZero, kAtomBytes);
           }
         }
         bulk_commit();
@@ -691,6 +698,7 @@ namespace mxq {
 int mx9_status_read(unsigned int* out, bool clear);      // mx9.cu
 int compose_status_read(unsigned int* out, bool clear);  // mxq_compose.cu
 int cols_status_read(unsigned int* out, bool clear);     // mx_cols_tma.cu
+int packed_status_read(unsigned int* out, bool clear);   // mx_packed.cu
 }
 
 // The device status word is the OR of the per-file words of the kernels.
@@ -707,9 +715,11 @@ extern "C" int mxq_device_status(uint32_t* out, int clear) {
   if (rc != MXQ_OK) return rc;
   rc = mxq::compose_status_read(&c, clear != 0);
   if (rc != MXQ_OK) return rc;
-  unsigned int t = 0;
+  unsigned int t = 0, k = 0;
   rc = mxq::cols_status_read(&t, clear != 0);
   if (rc != MXQ_OK) return rc;
-  *out = v | w | c | t;
+  rc = mxq::packed_status_read(&k, clear != 0);
+  if (rc != MXQ_OK) return rc;
+  *out = v | w | c | t | k;
   return MXQ_OK;
 }

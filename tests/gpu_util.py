@@ -2,6 +2,8 @@
 byte comparisons that name the first mismatch."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +17,7 @@ def require_gpu():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     from mx_block_quantization_gb300.build import build_library
-    build_library()
+    build_library(checked=os.environ.get("MXQ_CHECKED") == "1")  # the library lib() loads
     mxq.device_status(clear=True)
 
 

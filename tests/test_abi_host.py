@@ -41,6 +41,20 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_checked_twin_exports_the_same_and_says_so(L):
+    """libmxq_checked.so (bounds checks compiled in) has the same entry points;
+    mxq_debug_bounds tells the two apart without touching a GPU."""
+    import ctypes
+    if not mxq.CHECKED_LIB_PATH.exists():
+        from mx_block_quantization_gb300.build import build_library
+        build_library(checked=True)
+    C = ctypes.CDLL(str(mxq.CHECKED_LIB_PATH))
+    for name in _declared_functions():
+        assert hasattr(C, name), name
+    assert C.mxq_debug_bounds() == 1
+    assert L.mxq_debug_bounds() == 0
+
+
 def test_status_strings_and_version(L):
     for code in (mxq.OK, mxq.EBADSHAPE, mxq.EBADDTYPE, mxq.EBADOFFS, mxq.EALIGN, mxq.EOVERLAP,
                  mxq.ECUDA, mxq.ENULL):
