@@ -612,14 +612,20 @@ def run_case(args):
     build_library()
     M, N = (int(v) for v in args.shape.lower().split("x"))
     dev = torch.device("cuda", 0)
-    if args.case == "dual":
+    if args.case in ("dual", "dual3"):
+        # dual3: the three-pass composition (1x32 cast, 32x1 cast, K-groups swizzle)
         offs = None
         if args.groups:
             offs = torch.from_numpy(W.moe_group_offsets(args.groups, M // 128 - M // 1024)).to(dev)
         x = torch.from_numpy(W.normal_bf16((M, N), seed=0, scale=0.02).view(np.int16)).view(
             torch.bfloat16).to(dev)
+        out = mxq.quantize_2d_dual(x, offs)
+        ws = torch.empty(M * N // 32, dtype=torch.uint8, device=dev)
         for _ in range(args.warmup):
-            mxq.quantize_2d_dual(x, offs)
+            if args.case == "dual":
+                mxq.quantize_2d_dual(x, offs, out=out)
+            else:
+                mxq.quantize_2d_dual_3pass(x, offs, workspace=ws, out=out)
     elif args.case.startswith("rec_"):
         # the single packed tensor of MX9 (--fmt 9) or MX6 (--fmt 6) records, rows blocked
         tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
@@ -659,7 +665,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="also print one line per throughput-sweep shape (graph replay)")
-    ap.add_argument("--case", choices=["dual", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16",
+    ap.add_argument("--case", choices=["dual", "dual3", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16",
                                        "rec_pack_f32", "rec_pack_bf16", "rec_unpack_f32",
                                        "rec_unpack_bf16"],
                     help="only launch this kernel --warmup times on --shape (profiling)")
