@@ -336,7 +336,8 @@ __global__ void __launch_bounds__(kThreads)
     // copy in: 16-byte units, then 2-byte pieces
     const uint8_t* src = packed + r0 * RB;
     const int bytes = nvalid * RB;
-    const int n16 = in_buf(src, bytes, packed, static_cast<uint64_t>(nb) * RB, &g_packed_status) ? bytes >> 4 : 0;
+    const bool src_ok = in_buf(src, bytes, packed, static_cast<uint64_t>(nb) * RB, &g_packed_status);
+    const int n16 = src_ok ? bytes >> 4 : 0;
     uint4 v[kLoads];
 #pragma unroll
     for (int k = 0; k < kLoads; ++k) {
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads)
       const int i = lane + 32 * k;
       if (i < n16) sts128(st + 16u * i, v[k].x, v[k].y, v[k].z, v[k].w);
     }
-    for (int i = n16 * 8 + lane; i < (n16 ? bytes >> 1 : 0); i += 32) {
+    for (int i = n16 * 8 + lane; i < (src_ok ? bytes >> 1 : 0); i += 32) {
       const uint32_t h = __ldcs(reinterpret_cast<const uint16_t*>(src) + i);
       asm volatile("st.shared.u16 [%0], %1;" ::"r"(st + 2u * i), "r"(h) : "memory");
     }

@@ -93,6 +93,19 @@ def test_packed_cols_tma_tiles(fmt, dt, rows, cols, ld):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(1, 16), (129, 16), (1, 32), (257, 32), (128, 16)])
+def test_packed_last_group_of_few_records(fmt, dt, rows, cols):
+    """Contiguous whole-block rows through the record kernels where the last
+    group of 128 records holds one or two records (MX6: 12 or 24 bytes, less
+    than or not a multiple of a 16-byte unit), or the whole tensor is one record."""
+    x = W.mx9_outliers(rows, cols, seed=rows + cols, zero_blocks=0, tiny_blocks=0)
+    if dt == "bf16":
+        x = W.f32_to_bf16_bits(x)
+    _check(x, cols, fmt, 1, f"fmt{fmt} {dt} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("axis", [0, 1])
 def test_packed_outlier_workload(fmt, axis):
     """The [4096, 4096] outlier workload (zero and ~1e-40 blocks included)."""
