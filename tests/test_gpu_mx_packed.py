@@ -263,3 +263,26 @@ def test_packed_random_geometries(i):
     got = yflat.cpu().view(torch.int16 if is_bf16 else torch.int32).numpy()
     assert_bytes_equal(got[x_off:].view(np.uint8), ref.view(np.uint8), tag + " unpack")
     assert np.array_equal(got[:x_off], fill[:x_off].view(got.dtype)), tag + " before the view"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("rem", [1, 2, 3, 31, 33, 127])
+@pytest.mark.parametrize("pad", [0, 64])
+def test_packed_record_group_remainders(fmt, dt, rem, pad):
+    """Rows of an odd number c of whole blocks, with rows chosen so that the
+    block count leaves `rem` records in the last 128-record group (and so a
+    partial last run of the record pack's 32- and 128-block runs); pad 64: the
+    same with strided rows (c >= 129 blocks, the strided record kernels)."""
+    g = np.random.Generator(np.random.PCG64(97 * rem + 7 * pad + fmt + (dt == "bf16")))
+    c = int(g.integers(129, 320)) | 1 if pad else int(g.integers(1, 64)) * 2 + 1
+    rows = (rem * pow(c, -1, 128)) % 128 + 128 * int(g.integers(0, 3))
+    rows = rows or 128
+    assert (rows * c) % 128 == rem % 128
+    cols = 16 * c
+    x = np.zeros((rows, cols + pad), np.float32)
+    x[:, :cols] = W.mx9_outliers(rows, cols, seed=rem + rows, zero_blocks=0, tiny_blocks=0)
+    x[:, cols:] = np.float32(3e33)
+    if dt == "bf16":
+        x = W.f32_to_bf16_bits(x)
+    _check(x, cols, fmt, 1, f"fmt{fmt} {dt} {rows}x{cols}/{cols + pad} rem {rem}")
