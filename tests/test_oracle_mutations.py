@@ -64,9 +64,8 @@ def source():
     return open(SRC).read()
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(source, name, old, new):
-    assert source.count(old) == 1, f"mutation site not found or not unique: {name}"
+def _run_mutation(source: str, old: str, new: str):
+    """Build the oracle with one planted mistake and run the pins against it."""
     mutated = source.replace(old, new, 1)
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "mut.c")
@@ -75,8 +74,25 @@ def test_planted_mistake_is_caught(source, name, old, new):
         subprocess.run(["gcc", "-std=c11", "-O1", "-fPIC", "-shared", "-fno-fast-math",
                         "-ffp-contract=off", "-w", c, "-o", so, "-lm"], check=True)
         env = dict(os.environ, MXQ_ORACLE_LIB=so)
-        r = subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q", "-p", "no:cacheprovider",
-                            "-m", "not gpu"], cwd=ROOT, env=env, capture_output=True, text=True,
-                           timeout=600)
+        return subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q", "-p",
+                               "no:cacheprovider", "-m", "not gpu"], cwd=ROOT, env=env,
+                              capture_output=True, text=True, timeout=600)
+
+
+@pytest.fixture(scope="module")
+def results(source):
+    """Every mutation's pin run, several at a time (each is its own process)."""
+    from concurrent.futures import ThreadPoolExecutor
+    for name, old, _ in MUTATIONS:
+        assert source.count(old) == 1, f"mutation site not found or not unique: {name}"
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        futs = {name: ex.submit(_run_mutation, source, old, new) for name, old, new in MUTATIONS}
+        return {name: f.result() for name, f in futs.items()}
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(results, name, old, new):
+    r = results[name]
     assert r.returncode != 0, f"planted mistake '{name}' passed every pin"
     assert "failed" in r.stdout, r.stdout[-2000:]
