@@ -556,8 +556,22 @@ def run_sweep(mxq, torch, dev, rank):
             print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
     # the packed tensor in its other geometries: blocks along columns, and
-    # blocked rows at a pitch of cols + 64 (the input a strided view)
-    M, N = 16384, 8192
+    # blocked rows at a pitch of cols + 64 (the input a strided view), at a
+    # mid and a large shape
+    for M, N in ((16384, 8192), (32768, 16384)):
+        run_sweep_packed(mxq, torch, dev, rank, M, N, peak, kind)
+    if rank == 0:
+        geo = float(np.exp(np.mean(np.log(speedups))))
+        print(json.dumps({"sweep_summary": "fused dual-axis cast vs three-pass composition, "
+                          "CUDA-graph replay", "geomean_speedup": geo,
+                          "largest_shape_speedup": speedups[-1],
+                          "pages_figures": "2.6x geomean, 2.0x largest (GB200, 2062 MHz)"}),
+              flush=True)
+
+
+def run_sweep_packed(mxq, torch, dev, rank, M, N, peak, kind):
+    from mx_block_quantization_gb300 import workloads as W
+
     line = {"sweep_packed_geometries": [M, N], "peak_gbs": peak, "peak_kind": kind}
     for dt, tdt, esz in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
         wide = torch.from_numpy(W.normal_f32((M, N + 64), seed=0)).to(dev).to(tdt)
@@ -577,13 +591,6 @@ def run_sweep(mxq, torch, dev, rank):
     if rank == 0:
         print(json.dumps(line), flush=True)
     torch.cuda.empty_cache()
-    if rank == 0:
-        geo = float(np.exp(np.mean(np.log(speedups))))
-        print(json.dumps({"sweep_summary": "fused dual-axis cast vs three-pass composition, "
-                          "CUDA-graph replay", "geomean_speedup": geo,
-                          "largest_shape_speedup": speedups[-1],
-                          "pages_figures": "2.6x geomean, 2.0x largest (GB200, 2062 MHz)"}),
-              flush=True)
 
 
 def graph_time(torch, dev, launch, per_graph=20, replays=10):
