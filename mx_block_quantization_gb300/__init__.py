@@ -15,6 +15,15 @@ Operations (sources by page title):
 * :func:`mx9_pack` / :func:`mx9_unpack` -- AMD-AGI/ALTO PR #33 "mx9: add fused
   MX9 quantization kernel with pack/unpack": block 16, int8 q in [-127, 127],
   E8M0 shared exponent, one prime bit per pair.
+* :func:`mx_pack_packed` / :func:`mx_unpack_packed` -- the same page's later
+  commits: MX9 or MX6 records in one uint8 tensor, blocked along either axis of
+  a strided tensor, a partial last block zero-padded.
+* :func:`quantize_1x32`, :func:`quantize_32x1`, :func:`swizzle_kgroups`,
+  :func:`quantize_2d_dual_3pass` -- the three-pass composition the fused cast
+  replaces (pytorch/ao PR #4995, first paragraph), for comparison.
+
+With MXQ_CHECKED=1 in the environment the binding loads libmxq_checked.so,
+the same kernels with every computed global access tested against its buffer.
 """
 from __future__ import annotations
 
@@ -36,6 +45,7 @@ EALIGN = -4
 EOVERLAP = -5
 ECUDA = -6
 ENULL = -7
+ESCRATCH = -8
 F32 = 0
 BF16 = 1
 MAX_GROUPS = 1024
