@@ -55,7 +55,7 @@
 #ifndef MXQ_COLS_TMA_UNPACK_RING_KB
 #define MXQ_COLS_TMA_UNPACK_RING_KB 72
 #endif
-// tile orders (tile_at): tile rows per group, 1 = across a band of rows
+// unpack tile order (tile_at): tile rows per group, 1 = across a band of rows
 // first (x rows move as one run), 0 = down whole columns first (a column's
 // records move as one run)
 #ifndef MXQ_COLS_TMA_UNPACK_GROUP
@@ -63,12 +63,6 @@
 #endif
 #ifndef MXQ_COLS_TMA_UNPACK_GROUP_MX9_F32  // the MX9 fp32 unpack measured faster in groups
 #define MXQ_COLS_TMA_UNPACK_GROUP_MX9_F32 3
-#endif
-#ifndef MXQ_COLS_TMA_PACK_GROUP
-#define MXQ_COLS_TMA_PACK_GROUP 1
-#endif
-#ifndef MXQ_COLS_TMA_PACK_GROUP_MX9  // MX9 record runs start mid-sector on odd tile rows
-#define MXQ_COLS_TMA_PACK_GROUP_MX9 2
 #endif
 
 namespace {
@@ -94,16 +88,6 @@ struct ColsTma {
   static constexpr int kColsPerLane = 8 / kEsize;  // columns in 8 bytes of a row
   static constexpr int kRecord = kFmt == MXQ_FMT_MX9 ? MXQ_MX9_RECORD_BYTES : MXQ_MX6_RECORD_BYTES;
   static constexpr int kOffset = kFmt == MXQ_FMT_MX9 ? 6 : 3;
-  // pack tile order (tile_at): tile rows per group.  An MX9 run of 8
-  // records (144 bytes) starts 16 bytes into a 32-byte sector on every other
-  // tile row, so the two halves of such a sector come from tiles (tr, tc) and
-  // (tr + 1, tc); walking 2 tile rows at a time writes both halves together.
-  // In row-band order the halves of tens of thousands of sectors wait a whole
-  // wave apart: the bf16 MX9 pack fell to 4100-4180 GB/s at 32768x16384 (6430
-  // in pairs of rows, which cost 3.5% at 16384x8192); MX6 runs (96 bytes)
-  // never split a sector and keep the row-band order.
-  static constexpr int kPackGroup = kFmt == MXQ_FMT_MX9 ? MXQ_COLS_TMA_PACK_GROUP_MX9
-                                                        : MXQ_COLS_TMA_PACK_GROUP;
   // unpack tile order (tile_at): tile rows per group
   static constexpr int kUnpackGroup = kFmt == MXQ_FMT_MX9 && !kBF16 ? MXQ_COLS_TMA_UNPACK_GROUP_MX9_F32
                                                                     : MXQ_COLS_TMA_UNPACK_GROUP;
@@ -258,33 +242,38 @@ __device__ __forceinline__ bool consumers_sync_and(bool flag) {
   return r != 0;
 }
 
-// Tile t in the visiting order: kGroup tile rows at a time, column by column
-// inside a group (kGroup 1: across a band of rows first; 0: down whole
+// Tile t in the visiting order: `group` tile rows at a time, column by
+// column inside a group (group 1: across a band of rows first; 0: down whole
 // columns first).
-template <int kGroup>
-__device__ __forceinline__ void tile_at(int64_t t, int64_t tiles_r, int64_t tiles_c, int64_t* tr,
-                                        int64_t* tc) {
-  if (kGroup == 0) {
+__device__ __forceinline__ void tile_at_rows(int64_t t, int64_t tiles_r, int64_t tiles_c,
+                                             int64_t group, int64_t* tr, int64_t* tc) {
+  if (group == 0) {
     *tc = t / tiles_r;
     *tr = t - *tc * tiles_r;
-  } else if (kGroup == 1) {
+  } else if (group == 1) {
     *tr = t / tiles_c;
     *tc = t - *tr * tiles_c;
   } else {
-    const int64_t per_group = static_cast<int64_t>(kGroup) * tiles_c;
+    const int64_t per_group = group * tiles_c;
     const int64_t g = t / per_group;
     const int64_t local = t - g * per_group;
-    const int64_t rows = tiles_r - g * kGroup < kGroup ? tiles_r - g * kGroup : kGroup;
-    *tr = g * kGroup + local % rows;
+    const int64_t rows = tiles_r - g * group < group ? tiles_r - g * group : group;
+    *tr = g * group + local % rows;
     *tc = local / rows;
   }
+}
+
+template <int kGroup>
+__device__ __forceinline__ void tile_at(int64_t t, int64_t tiles_r, int64_t tiles_c, int64_t* tr,
+                                        int64_t* tc) {
+  tile_at_rows(t, tiles_r, tiles_c, kGroup, tr, tc);
 }
 
 template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_pack_cols_tma_kernel(const __grid_constant__ CUtensorMap tm_x,
                             const __grid_constant__ CUtensorMap tm_rec, int32_t tiles_r,
-                            int32_t tiles_c) {
+                            int32_t tiles_c, int32_t group) {
   using C = ColsTma<kBF16, kFmt>;
   using R = MxRule<C::kOffset, C::kQMax>;
   constexpr int kStages = C::kPackStages;
@@ -312,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              abort_flag, &g_cols_status, MXQ_DEV_TIMEOUT))
         break;
       int64_t tr, tc;
-      tile_at<C::kPackGroup>(blockIdx.x + i * static_cast<int64_t>(gridDim.x), tiles_r, tiles_c, &tr, &tc);
+      tile_at_rows(blockIdx.x + i * static_cast<int64_t>(gridDim.x), tiles_r, tiles_c, group, &tr, &tc);
       mbar_arrive_expect_tx(bars.full(s), kTileBytes);
 #pragma unroll
       for (int b = 0; b < kBoxes; ++b)
@@ -336,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              &g_cols_status, MXQ_DEV_TIMEOUT))
         break;
       int64_t tr, tc;
-      tile_at<C::kPackGroup>(blockIdx.x + i * static_cast<int64_t>(gridDim.x), tiles_r, tiles_c, &tr, &tc);
+      tile_at_rows(blockIdx.x + i * static_cast<int64_t>(gridDim.x), tiles_r, tiles_c, group, &tr, &tc);
       tma_store_2d(&tm_rec, static_cast<int32_t>(tr * C::kRunBytes),
                    static_cast<int32_t>(tc * C::kTileCols), rec_base + ob * C::kRecTileBytes);
       bulk_commit();
@@ -572,6 +561,20 @@ int launch_wave(uint32_t smem, int64_t tiles, int threads, cudaStream_t stream, 
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 
+// Tile rows per group of the pack's tile order.  An MX9 run of 8 records (144
+// bytes) starts 16 bytes into a 32-byte sector on every other tile row, so the
+// two halves of such a sector come from tiles (tr, tc) and (tr + 1, tc).  In
+// row-band order the bf16 MX9 pack fell to 4100-4180 GB/s at 32768x16384 and
+// 5263 at 24576x16384 (6430 walking pairs of tile rows), while at 8192 columns
+// the row-band order measured best (pairs cost 3.5%): pairs from 16384 columns
+// on, measured; fp32 MX9 measured as well or better in pairs at every size;
+// MX6 runs (96 bytes) never split a sector and keep the row-band order.
+template <bool kBF16, int kFmt>
+int pack_group(int64_t cols) {
+  if (kFmt != MXQ_FMT_MX9) return 1;
+  return kBF16 && cols <= 8192 ? 1 : 2;
+}
+
 template <bool kBF16, int kFmt>
 int launch_pack(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* packed,
                 cudaStream_t stream) {
@@ -582,7 +585,8 @@ int launch_pack(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* 
   const int64_t tiles_c = (cols + C::kTileCols - 1) / C::kTileCols;
   return launch_wave<mx_pack_cols_tma_kernel<kBF16, kFmt>>(
       C::kPackSmem, tiles_r * tiles_c, kThreads, stream, tm_x, tm_rec,
-      static_cast<int32_t>(tiles_r), static_cast<int32_t>(tiles_c));
+      static_cast<int32_t>(tiles_r), static_cast<int32_t>(tiles_c),
+      static_cast<int32_t>(pack_group<kBF16, kFmt>(cols)));
 }
 
 template <bool kBF16, int kFmt>
