@@ -12,8 +12,9 @@
 // Finite blocks round with one FMA: for |v| < 2^22, 1.5 * 2^23 + v rounds once,
 // half to even, to an integer whose two's-complement value is the low 16 bits
 // of the result (a finite block gives |x / 2^k| < 2^8).  Two elements are then
-// clamped at once as an int16 pair.  Blocks holding Inf or NaN (exponent field
-// 255) take the general path: cvt.rni gives 0 for NaN and saturates +-Inf.
+// clamped at once as an int16 pair.  MX6 blocks of bf16 round in packed bf16
+// instead (q_pair_bf16x2).  Blocks holding Inf or NaN (exponent field 255) take
+// the general path: cvt.rni gives 0 for NaN and saturates +-Inf.
 #pragma once
 
 #include <stdint.h>
@@ -46,6 +47,8 @@ template <int kOff, int kQMax>
 struct MxRule {
   static constexpr uint32_t kClampLo = static_cast<uint32_t>(static_cast<uint16_t>(-kQMax)) * 0x10001u;
   static constexpr uint32_t kClampHi = static_cast<uint32_t>(kQMax) * 0x10001u;
+  // bf16 input of a 5-bit format: one packed bf16 FMA per pair (q_pair_bf16x2)
+  static constexpr bool kPackedBf16 = kQMax == 15;
 
   // 2^-k of a pair from the block's exponent field eb8 (E = eb8 - 127) and the
   // pair's prime bit t: 127 - k = min(254 + kOff - eb8 + t, 253).
@@ -79,6 +82,20 @@ struct MxRule {
         : "=f"(ra), "=f"(rb)
         : "r"(w), "r"(mult_bits), "f"(12582912.0f));
     return clamp_pair(__byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x5410));
+  }
+
+  // MX6 of bf16 (|x / 2^k| < 16 in a finite block): one packed bf16 FMA per
+  // pair, against two mixed-precision FMAs and a byte permute.  192 + v stays in the binade [128, 256), where the bf16 step is 1,
+  // so x * 2^-k + 192 rounds once, half to even, to 192 + round(v); as bits
+  // that is 0x4340 + round(v), whose low five bits are the two's-complement
+  // code (0x4340 is a multiple of 32).  Only +-16 needs the clamp to +-15.
+  // mult2: the power-of-two multiplier as bf16 in both halves.
+  static __device__ __forceinline__ uint32_t q_pair_bf16x2(uint32_t w, uint32_t mult2) {
+    uint32_t r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(mult2), "r"(0x43404340u));
+    asm("max.s16x2 %0, %0, %1;" : "+r"(r) : "r"(0x43314331u));  // 192 - 15
+    asm("min.s16x2 %0, %0, %1;" : "+r"(r) : "r"(0x434F434Fu));  // 192 + 15
+    return r;
   }
 
   // General path for one element: x * 2^-k (exact, no flush), cvt.rni, clamp.
@@ -120,7 +137,9 @@ struct MxRule {
     *bits_out = bits;
   }
 
-  // 16 bf16 elements as 8 words (word p = pair p, element 2p in the low half).
+  // 16 bf16 elements as 8 words (word p = pair p, element 2p in the low half)
+  // -> h as in block_f32 for MX9; for MX6 each half of h is 192 + q as bf16
+  // bits, whose low five bits are the code.
   // Exponent fields are compared in place, two per word: with e16 = block
   // field << 7, the low half of (w & 0x7F80) + 0x8000 - e16 reaches bit 15
   // exactly when the element's field is >= the block's, likewise the high
@@ -147,12 +166,17 @@ struct MxRule {
     }
     const uint32_t d2 = (0x8000u - e16) * 0x10001u;
     const float m0 = multiplier(eb8, 0u), m1 = multiplier(eb8, 1u);
+    const uint32_t mult0 = kPackedBf16 ? (__float_as_uint(m0) >> 16) * 0x10001u : __float_as_uint(m0);
+    const uint32_t dmult = (kPackedBf16 ? (__float_as_uint(m1) >> 16) * 0x10001u : __float_as_uint(m1)) - mult0;
     uint32_t bits = 0;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-      const uint32_t t = ((m[p] + d2) & 0x80008000u) == 0u;
-      bits |= t << p;
-      h[p] = q_pair_bf16(w[p], __float_as_uint(t ? m1 : m0));
+      const bool keep = ((m[p] + d2) & 0x80008000u) != 0u;
+      const uint32_t t = keep ? 0u : 1u;
+      // prime bit and multiplier as integer multiply-adds, off the ALU pipe
+      bits = mad_u32(t, 1u << p, bits);
+      const uint32_t mult = mad_u32(t, dmult, mult0);
+      h[p] = kPackedBf16 ? q_pair_bf16x2(w[p], mult) : q_pair_bf16(w[p], mult);
     }
     *eb8_out = eb8;
     *bits_out = bits;
@@ -169,8 +193,9 @@ __device__ __forceinline__ uint4 pairs_to_bytes(const uint32_t* h) {
 }
 
 
-// 8 int16 pairs with values in [-15, 15] -> the 80 bits of sixteen 5-bit
-// two's-complement codes, element i at bits 5i..5i+4: bits 0-31, 32-63 and
+// 8 pairs of 16-bit halves whose low five bits are the 5-bit two's-complement
+// codes (an int16 in [-15, 15], or 192 + q as bf16 bits) -> the 80 bits of the
+// sixteen codes, element i at bits 5i..5i+4: bits 0-31, 32-63 and
 // 64-79 (low half of *hi).  The disjoint fields are summed with multiply-adds,
 // which leave the integer ALU pipe (the MX6 bf16 pack's limit) to the rest:
 // measured +0.9% over shifts and ORs.
