@@ -15,7 +15,8 @@
 // prime byte with coalesced stores.  Finite blocks round with one FMA against
 // 1.5 * 2^23 and clamp two elements at once as int16 pairs; bf16 blocks take
 // their exponent maximum on the packed words and feed the bf16 halves to a
-// mixed-precision FMA, which keeps the integer pipe (the limit for bf16) light.
+// mixed-precision FMA (MX6: one packed bf16 FMA per pair), which keeps the
+// integer pipe (the limit for bf16) light.
 // The same kernel writes the packed MX9 / MX6 record forms of mx_packed.cu
 // (blocked rows read at a pitch: one bulk copy per row piece of a stage),
 // staging each warp's 32 records and storing them with one bulk copy.
