@@ -21,6 +21,9 @@ public dataset):
 * ``moe_grouped``     -- [65536, 7168] bf16 N(0,1) * 0.02, 64 expert groups of
   128 * Multinomial(448, 1/64) rows: offs[-1] = 57344, an 8192-row uncovered
   tail; some groups can be empty.
+* ``tiny_exponents``  -- blocks at the scale exponent's floor: zeros,
+  subnormals and the smallest normals (exponent field <= a per-16x16-tile cap
+  in 0..8), fp32 or bf16 bit patterns.
 * ``SWEEP_SHAPES``    -- throughput sweep shapes, N(0,1).
 """
 from __future__ import annotations
@@ -144,3 +147,24 @@ def mx9_outliers(rows: int = 4096, cols: int = 4096, seed: int = SEED,
 
 def mx9_outliers_bf16(rows: int = 4096, cols: int = 4096, seed: int = SEED) -> np.ndarray:
     return f32_to_bf16_bits(mx9_outliers(rows, cols, seed))
+
+
+def tiny_exponents(rows: int, cols: int, bf16: bool, seed: int = SEED) -> np.ndarray:
+    """Every element zero, subnormal or a normal with exponent field 1..cap,
+    random sign and mantissa, cap drawn from 0..8 per 16x16 tile (0: subnormals
+    only), so that every 16-block along either axis has its largest field at 8
+    or below; 10% of mantissas sit at exactly half of their step's range (bf16
+    0x40, fp32 1 << 22).  fp32 as float32, bf16 as uint16 bit patterns."""
+    g = rng(seed)
+    cap = np.repeat(np.repeat(g.integers(0, 9, (rows // 16 + 1, cols // 16 + 1)), 16, 0), 16, 1)
+    cap = cap[:rows, :cols]
+    normal = (g.random((rows, cols)) >= 0.6) & (cap > 0)
+    field = np.where(normal, 1 + (g.random((rows, cols)) * np.maximum(cap, 1)).astype(np.int64), 0)
+    sign = g.integers(0, 2, (rows, cols))
+    if bf16:
+        mant = g.integers(0, 128, (rows, cols))
+        mant[g.random((rows, cols)) < 0.1] = 64
+        return ((sign << 15) | (field << 7) | mant).astype(np.uint16)
+    mant = g.integers(0, 1 << 23, (rows, cols))
+    mant[g.random((rows, cols)) < 0.1] = 1 << 22
+    return ((sign << 31) | (field << 23) | mant).astype(np.uint32).view(np.float32)

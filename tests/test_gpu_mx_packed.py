@@ -121,29 +121,6 @@ def test_packed_every_bf16_pattern(fmt):
     _check(x, 256, fmt, 0, f"fmt{fmt} bf16 patterns axis0")
 
 
-def _tiny_exponent_tensor(rows: int, cols: int, bf16: bool, seed: int) -> np.ndarray:
-    """Every element zero, subnormal or a normal with exponent field 1..cap, random
-    sign and mantissa, cap drawn from 0..8 per 16x16 tile (0: subnormals only):
-    every block's largest field is at most 8, so the scale exponent sits at or
-    near its floor of -126 and subnormals round to 0 or +-1 (a subnormal at
-    exactly half a step ties to 0)."""
-    g = np.random.Generator(np.random.PCG64(seed))
-    cap = np.repeat(np.repeat(g.integers(0, 9, (rows // 16 + 1, cols // 16 + 1)), 16, 0), 16, 1)
-    cap = cap[:rows, :cols]
-    normal = (g.random((rows, cols)) >= 0.6) & (cap > 0)
-    field = np.where(normal, 1 + (g.random((rows, cols)) * np.maximum(cap, 1)).astype(np.int64), 0)
-    sign = g.integers(0, 2, (rows, cols))
-    if bf16:
-        mant = g.integers(0, 128, (rows, cols))
-        mant[g.random((rows, cols)) < 0.1] = 64        # half a step at the floor
-        bits = (sign << 15) | (field << 7) | mant
-        return bits.astype(np.uint16)
-    mant = g.integers(0, 1 << 23, (rows, cols))
-    mant[g.random((rows, cols)) < 0.1] = 1 << 22
-    bits = (sign << 31) | (field << 23) | mant
-    return bits.astype(np.uint32).view(np.float32)
-
-
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("axis", [0, 1])
@@ -151,7 +128,7 @@ def _tiny_exponent_tensor(rows: int, cols: int, bf16: bool, seed: int) -> np.nda
 def test_packed_tiny_exponent_blocks(fmt, dt, axis, rows, cols):
     """Blocks of subnormals and the smallest normals, where the scale exponent is
     clamped at -126 and a subnormal element can round to a nonzero code."""
-    x = _tiny_exponent_tensor(rows, cols, dt == "bf16", seed=rows + 7 * axis + fmt)
+    x = W.tiny_exponents(rows, cols, dt == "bf16", seed=rows + 7 * axis + fmt)
     _check(x, cols, fmt, axis, f"fmt{fmt} {dt} axis{axis} tiny {rows}x{cols}")
 
 

@@ -56,6 +56,12 @@ MUTATIONS = [
     ("packed record fields swapped", "        mx_block(v, t, fmt, &rec[0], &rec[1], q);", "        mx_block(v, t, fmt, &rec[1], &rec[0], q);"),
     ("axis-0 index transposed", "int64_t idx = axis == 1 ? line * ld + pos : pos * ld + line;",
      "int64_t idx = axis == 1 ? line * ld + pos : line * ld + pos;"),
+    ("packed pack no -126 clamp", "        int k = E - d - tau;\n        if (k < -126) k = -126;\n",
+     "        int k = E - d - tau;\n"),
+    ("packed pack ties away from zero", "            r = nearbyint(ldexp(v[i], -k));",
+     "            r = round(ldexp(v[i], -k));"),
+    ("packed unpack no -126 clamp", "            k = E - d - tau;\n            if (k < -126) k = -126;\n",
+     "            k = E - d - tau;\n"),
 ]
 
 

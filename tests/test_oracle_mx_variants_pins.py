@@ -171,3 +171,36 @@ def test_every_mx6_code_round_trips():
     codes = _mx6_codes(rec).reshape(-1)
     np.testing.assert_array_equal(codes[1:pairs.size:2], qs)
     np.testing.assert_array_equal(oracle.mx_unpack(rec, oracle.MX6, 4, 16, "f32"), x)
+
+
+@pytest.mark.parametrize("fmt,off,qmax", [(oracle.MX9, 6, 127), (oracle.MX6, 3, 15)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_brute_force_at_the_exponent_floor(fmt, off, qmax, bf16):
+    """Blocks of zeros, subnormals and the smallest normals (every largest field
+    <= 8), where k = max(E - off - prime, -126) sits at or near its floor and a
+    subnormal rounds to 0 or +-1: exponent byte, prime bits and each q as the
+    nearest grid point (ties to even), from math.frexp on the exact input; the
+    unpack returns q * 2^k exactly (|q| * 2^k is 0 or at least 2^-126)."""
+    x = W.tiny_exponents(32, 64, bf16, seed=17 + fmt)
+    v = W.bf16_bits_to_f32(x) if bf16 else x
+    rec = oracle.mx_pack(x, fmt)
+    y = oracle.mx_unpack(rec, fmt, 32, 64, "f32").reshape(-1, 16).astype(np.float64)
+    q = _mx6_codes(rec) if fmt == oracle.MX6 else rec[:, 2:].view(np.int8).astype(np.int64)
+    grid = np.arange(-qmax, qmax + 1)
+    blocks = v.reshape(-1, 16).astype(np.float64)
+    floor_hits = 0
+    for b in range(blocks.shape[0]):
+        t = [_t(float(e)) for e in blocks[b]]
+        E = max(t)
+        assert rec[b, 0] == E + 127
+        for i in range(16):
+            tau = int(max(t[2 * (i // 2)], t[2 * (i // 2) + 1]) < E)
+            assert (rec[b, 1] >> (i // 2)) & 1 == tau
+            k = max(E - off - tau, -126)
+            floor_hits += k == -126
+            d = np.abs(grid * 2.0 ** k - blocks[b, i])
+            best = grid[d == d.min()]
+            want = best[0] if best.size == 1 else best[best % 2 == 0][0]
+            assert q[b, i] == want, (b, i, blocks[b, i], k)
+            assert y[b, i] == want * 2.0 ** k, (b, i, y[b, i], k)
+    assert floor_hits > 100

@@ -1,5 +1,6 @@
 """The seeded input generators produce the published workload recipes, deterministically."""
 import numpy as np
+import pytest
 
 from mx_block_quantization_gb300 import workloads as W
 
@@ -46,3 +47,18 @@ def test_mx9_recipe_counts():
     tiny = (np.abs(blocks).max(axis=1) > 0) & (np.abs(blocks).max(axis=1) < 1e-37)
     assert tiny.sum() == 64
     assert (np.abs(x) > 20).mean() > 0.005
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_tiny_exponents_recipe(bf16):
+    x = W.tiny_exponents(256, 320, bf16, seed=3)
+    assert np.array_equal(x.view(np.uint8), W.tiny_exponents(256, 320, bf16, seed=3).view(np.uint8))
+    bits = x.astype(np.uint32) if bf16 else x.view(np.uint32)
+    field = (bits >> 7) & 0xFF if bf16 else (bits >> 23) & 0xFF
+    assert field.max() <= 8
+    tiles = field.reshape(16, 16, 20, 16).max(axis=(1, 3))   # largest field per 16x16 tile
+    assert (tiles == 0).any() and (tiles == 8).any()          # subnormal-only tiles and the cap
+    half = 0x40 if bf16 else 1 << 22
+    mant = bits & (0x7F if bf16 else 0x7FFFFF)
+    assert 0.08 < (mant == half).mean() < 0.14
+    assert 0.5 < (field == 0).mean() < 0.8
