@@ -85,10 +85,11 @@ struct MxRule {
   }
 
   // MX6 of bf16 (|x / 2^k| < 16 in a finite block): one packed bf16 FMA per
-  // pair, against two mixed-precision FMAs and a byte permute.  192 + v stays in the binade [128, 256), where the bf16 step is 1,
-  // so x * 2^-k + 192 rounds once, half to even, to 192 + round(v); as bits
-  // that is 0x4340 + round(v), whose low five bits are the two's-complement
-  // code (0x4340 is a multiple of 32).  Only +-16 needs the clamp to +-15.
+  // pair, against two mixed-precision FMAs and a byte permute.  192 + v stays
+  // in the binade [128, 256), where the bf16 step is 1, so x * 2^-k + 192
+  // rounds once, half to even, to 192 + round(v); as bits that is
+  // 0x4340 + round(v), whose low five bits are the two's-complement code
+  // (0x4340 is a multiple of 32).  Only +-16 needs the clamp to +-15.
   // mult2: the power-of-two multiplier as bf16 in both halves.
   static __device__ __forceinline__ uint32_t q_pair_bf16x2(uint32_t w, uint32_t mult2) {
     uint32_t r;
@@ -138,8 +139,8 @@ struct MxRule {
   }
 
   // 16 bf16 elements as 8 words (word p = pair p, element 2p in the low half)
-  // -> h as in block_f32 for MX9; for MX6 each half of h is 192 + q as bf16
-  // bits, whose low five bits are the code.
+  // -> h as in block_f32, except that for a finite MX6 block each half of h
+  // is 192 + q as bf16 bits, whose low five bits are the code.
   // Exponent fields are compared in place, two per word: with e16 = block
   // field << 7, the low half of (w & 0x7F80) + 0x8000 - e16 reaches bit 15
   // exactly when the element's field is >= the block's, likewise the high
