@@ -19,7 +19,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "mxq_oracle.c")
 PINS = ["tests/test_oracle_mxfp8_pins.py", "tests/test_oracle_mx9_pins.py",
-        "tests/test_oracle_mx_variants_pins.py"]
+        "tests/test_oracle_mx_variants_pins.py", "tests/test_oracle_dual_twin.py"]
 
 MUTATIONS = [
     ("E4M3 max 480 instead of 448", "amax <= ldexp(448.0, mid - 127)", "amax <= ldexp(480.0, mid - 127)"),
