@@ -611,7 +611,8 @@ extern "C" int mxq_quantize_2d_dual_rows(const void* x, int64_t rows, int64_t N,
   if (rc != MXQ_OK) return rc;
   rc = check_shape(M, N);
   if (rc != MXQ_OK) return rc;
-  if (row0 < 0 || row0 % kTile != 0 || row0 + rows > M) return MXQ_EBADSHAPE;
+  // the band inside [0, M), with no int64 sum that could wrap for a far row0
+  if (row0 < 0 || row0 % kTile != 0 || row0 > M || rows > M - row0) return MXQ_EBADSHAPE;
   if (offs == nullptr ? G != 0 : (G < 1 || G > MXQ_MAX_GROUPS)) return MXQ_EBADOFFS;
   if (offs != nullptr && !aligned_to(offs, 4)) return MXQ_EALIGN;
   if (rows == 0 || N == 0) return MXQ_OK;

@@ -28,7 +28,7 @@ L = mxq.lib()
 vp = ctypes.c_void_p
 I64_MAX = (1 << 63) - 1
 EDGE = [0, 1, 15, 16, 17, 31, 32, 127, 128, 129, 256, 4096, 8192 + 128, (1 << 31) - 1, 1 << 31,
-        (1 << 31) + 128, 1 << 40, 1 << 62, I64_MAX, -1, -128, -(1 << 62)]
+        (1 << 31) + 128, 1 << 40, 1 << 62, I64_MAX - 127, I64_MAX, -1, -128, -(1 << 62)]
 g = np.random.Generator(np.random.PCG64(20261202))
 BASE = [(k + 1) << 56 for k in range(8)]  # buffers 2^56 bytes apart
 def pick():
@@ -52,6 +52,28 @@ for _ in range(N_CASES):
     else:
         want = {mxq.ECUDA, mxq.EOVERLAP}
     expect("dual", rc, want, (M, N))
+    dual_shape = ok_shape
+    # the single-axis casts and the three passes take the same shapes
+    rc = L.mxq_quantize_1x32(vp(BASE[0]), M, N, vp(BASE[1]), vp(BASE[2]), None)
+    expect("1x32", rc, want, (M, N))
+    rc = L.mxq_quantize_32x1(vp(BASE[0]), M, N, vp(BASE[3]), vp(BASE[4]), None)
+    expect("32x1", rc, want, (M, N))
+    rc = L.mxq_swizzle_kgroups(vp(BASE[4]), N, M, None, 0, vp(BASE[5]), None)
+    expect("swizzle", rc, want, (M, N))
+    ws = pick()
+    rc = L.mxq_quantize_2d_dual_3pass(vp(BASE[0]), M, N, None, 0, vp(BASE[1]), vp(BASE[2]),
+                                      vp(BASE[3]), vp(BASE[4]), vp(BASE[6]), ws, None)
+    want3 = want if not dual_shape or M * N == 0 else \
+        ({mxq.EBADSHAPE} if ws < 0 or ws < M * N // 32 else want)
+    expect("3pass", rc, want3, (M, N, ws))
+    # one band [row0, row0 + rows) of an M-row matrix
+    rows, row0 = pick(), pick()
+    rc = L.mxq_quantize_2d_dual_rows(vp(BASE[0]), rows, N, row0, M, None, 0, vp(BASE[1]),
+                                     vp(BASE[2]), vp(BASE[3]), vp(BASE[4]), None)
+    shape_ok = lambda a: a >= 0 and a % 128 == 0 and a <= (1 << 31) - 1
+    band_ok = shape_ok(rows) and dual_shape and row0 >= 0 and row0 % 128 == 0 and row0 + rows <= M
+    wantr = {mxq.EBADSHAPE} if not band_ok else {mxq.OK} if rows * N == 0 else {mxq.ECUDA, mxq.EOVERLAP}
+    expect("dual_rows", rc, wantr, (rows, N, row0, M))
     # split MX9 pack and unpack
     rows, cols, dt = pick(), pick(), int(g.integers(0, 2))
     rc = L.mx9_pack(vp(BASE[0]), dt, rows, cols, vp(BASE[1]), vp(BASE[2]), vp(BASE[3]), None)
@@ -72,6 +94,12 @@ for _ in range(N_CASES):
     expect("mx_pack_packed", rc, want, (rows, cols, ld, axis, fmt, dt))
     rc = L.mx_unpack_packed(vp(BASE[1]), fmt, vp(BASE[0]), dt, rows, cols, ld, axis, None)
     expect("mx_unpack_packed", rc, want, (rows, cols, ld, axis, fmt, dt))
+# bands placed past int64 range by their start (row0 + rows would wrap)
+for row0 in (I64_MAX - 127, I64_MAX - 255, (1 << 62) + 128, (1 << 31) * 128):
+    for rows in (128, 256, 1 << 30):
+        rc = L.mxq_quantize_2d_dual_rows(vp(BASE[0]), rows, 128, row0, 1 << 20, None, 0, vp(BASE[1]),
+                                         vp(BASE[2]), vp(BASE[3]), vp(BASE[4]), None)
+        expect("dual_rows far row0", rc, {mxq.EBADSHAPE}, (rows, row0))
 print("SEEN", seen.get(mxq.EBADSHAPE, 0), seen.get(mxq.OK, 0), seen.get(mxq.ECUDA, 0))
 print("BAD", len(bad))
 for b in bad[:20]:

@@ -203,6 +203,7 @@ def test_dual_rows_rejections_before_any_cuda_call(L):
     assert call(row0=64) == mxq.EBADSHAPE           # band start not a multiple of 128
     assert call(row0=512) == mxq.EBADSHAPE          # band past the tensor
     assert call(rows=256, row0=384) == mxq.EBADSHAPE
+    assert call(row0=(1 << 63) - 128) == mxq.EBADSHAPE  # row0 + rows would wrap int64
     assert call(M=500) == mxq.EBADSHAPE
     assert call(rows=0) == mxq.OK                    # empty band: nothing to do
     assert call(x=0) == mxq.ENULL
