@@ -26,6 +26,10 @@ sys.path.insert(0, ROOT)
 import mx_block_quantization_gb300 as mxq
 L = mxq.lib()
 vp = ctypes.c_void_p
+# not wrapped by the binding: declared here so 64-bit sizes pass unchanged
+L.mxq_quantize_2d_dual_3pass_noalloc.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp,
+                                                 ctypes.c_int32, vp, vp, vp, vp, vp]
+L.mxq_quantize_2d_dual_3pass_noalloc.restype = ctypes.c_int
 I64_MAX = (1 << 63) - 1
 EDGE = [0, 1, 15, 16, 17, 31, 32, 127, 128, 129, 256, 4096, 8192 + 128, (1 << 31) - 1, 1 << 31,
         (1 << 31) + 128, 1 << 40, 1 << 62, I64_MAX - 127, I64_MAX, -1, -128, -(1 << 62)]
@@ -66,6 +70,11 @@ for _ in range(N_CASES):
     want3 = want if not dual_shape or M * N == 0 else \
         ({mxq.EBADSHAPE} if ws < 0 or ws < M * N // 32 else want)
     expect("3pass", rc, want3, (M, N, ws))
+    rc = L.mxq_quantize_2d_dual_3pass_noalloc(vp(BASE[0]), M, N, None, 0, vp(BASE[1]), vp(BASE[2]),
+                                              vp(BASE[3]), vp(BASE[4]), None)
+    wantn = want if not dual_shape or M * N == 0 else \
+        ({mxq.ESCRATCH} if M * N // 32 > (16 << 20) else want)
+    expect("3pass_noalloc", rc, wantn, (M, N))
     # one band [row0, row0 + rows) of an M-row matrix
     rows, row0 = pick(), pick()
     rc = L.mxq_quantize_2d_dual_rows(vp(BASE[0]), rows, N, row0, M, None, 0, vp(BASE[1]),
