@@ -22,7 +22,11 @@ struct ByteRange {
   uint64_t bytes;
 };
 
+// A range that wraps past the top of the address space is no real buffer and
+// counts as overlapping.
 inline bool ranges_overlap(const ByteRange* r, int n) {
+  for (int i = 0; i < n; ++i)
+    if (r[i].bytes != 0 && r[i].lo + r[i].bytes <= r[i].lo) return true;
   for (int i = 0; i < n; ++i) {
     if (r[i].bytes == 0) continue;
     for (int j = i + 1; j < n; ++j) {

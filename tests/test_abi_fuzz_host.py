@@ -109,6 +109,16 @@ for row0 in (I64_MAX - 127, I64_MAX - 255, (1 << 62) + 128, (1 << 31) * 128):
         rc = L.mxq_quantize_2d_dual_rows(vp(BASE[0]), rows, 128, row0, 1 << 20, None, 0, vp(BASE[1]),
                                          vp(BASE[2]), vp(BASE[3]), vp(BASE[4]), None)
         expect("dual_rows far row0", rc, {mxq.EBADSHAPE}, (rows, row0))
+# a buffer whose byte range would wrap past the top of the address space
+TOP = (1 << 64) - 4096
+for M, N in ((128, 128), (1024, 4096)):
+    rc = L.mxq_quantize_2d_dual(vp(TOP), M, N, None, 0, vp(BASE[1]), vp(BASE[2]), vp(BASE[3]),
+                                vp(BASE[4]), None)
+    expect("dual wrapped x", rc, {mxq.EOVERLAP}, (M, N))
+    rc = L.mx9_pack(vp(BASE[0]), 0, M, N, vp(TOP), vp(BASE[2]), vp(BASE[3]), None)
+    expect("mx9_pack wrapped q", rc, {mxq.EOVERLAP}, (M, N))
+    rc = L.mx_pack_packed(vp(TOP), 0, M, N, N, 1, 9, vp(BASE[1]), None)
+    expect("mx_pack_packed wrapped x", rc, {mxq.EOVERLAP}, (M, N))
 print("SEEN", seen.get(mxq.EBADSHAPE, 0), seen.get(mxq.OK, 0), seen.get(mxq.ECUDA, 0))
 print("BAD", len(bad))
 for b in bad[:20]:
