@@ -39,11 +39,11 @@ typedef struct CUstream_st *cudaStream_t;
 
 /* ---- status codes ------------------------------------------------------ */
 #define MXQ_OK 0
-#define MXQ_EBADSHAPE (-1) /* a size is negative or violates the method's multiples */
+#define MXQ_EBADSHAPE (-1) /* a size is negative, too large, or violates the method's multiples */
 #define MXQ_EBADDTYPE (-2) /* dtype code is not MXQ_F32 / MXQ_BF16 */
 #define MXQ_EBADOFFS (-3)  /* group count out of range, or offs/G inconsistent */
 #define MXQ_EALIGN (-4)    /* a pointer is not 16-byte aligned (offs: 4-byte) */
-#define MXQ_EOVERLAP (-5)  /* two buffers' byte ranges overlap, or one wraps past the top of the address space */
+#define MXQ_EOVERLAP (-5)  /* two buffers' byte ranges overlap (or one wraps past the top of memory) */
 #define MXQ_ECUDA (-6)     /* the CUDA runtime refused the launch */
 #define MXQ_ENULL (-7)     /* a required pointer is NULL */
 #define MXQ_ESCRATCH (-8)  /* needs more than the static scratch of the no-allocation call */
