@@ -1,17 +1,23 @@
 """Benchmark of the MX block-quantization hot path on GB300.
 
 One step = one pass of the whole path over one batch of synthetic input:
-  1. mxq_quantize_2d_dual on the MoE-grouped bf16 [65536, 7168] tensor
+  1. mx9_pack of an fp32 [16384, 8192] N(0,1) tensor;
+  2. mxq_quantize_2d_dual on the MoE-grouped bf16 [65536, 7168] tensor
      (64 K-groups, offs[-1] = 57344, 8192-row uncovered tail);
-  2. mx9_pack of an fp32 [16384, 8192] N(0,1) tensor;
-  3. mx9_unpack of its packed parts back to fp32.
-Throughput = algorithmic bytes of the step (4.0625 B per element for the dual
-cast; 5.125 B per element for each MX9 pass on fp32) / device time.  Inputs
-are larger than the 129 MB L2, so no flush is needed between steps.
+  3. mx9_unpack of the packed parts of step 1 back to fp32.
+The warm-up replays a one-step CUDA graph; the timed region replays, once, a
+graph of the K steps (three kernel nodes each, programmatic dependent launch
+between consecutive kernels) between one pair of events.  Throughput = algorithmic bytes of the step
+(4.0625 B per element for the dual cast; 5.125 B per element for each MX9
+pass on fp32) / device time.  Inputs are larger than the 129 MB L2, so no
+flush is needed between steps.  Per-kernel figures come from separate passes
+after the timed region, and the `configs` key holds the graph-replay rates of
+every other workload (the 128x128 case, the MX9 outlier tensor, the specials
+tensor, the throughput sweep with the three-pass speedup, the packed forms).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on the
 host cores instead, on bounded samples of the same workload.  `--sweep` prints
-one extra line per throughput-sweep shape, timed under CUDA-graph replay.
+one extra line per packed-tensor geometry, timed under CUDA-graph replay.
 
 Multi-GPU (torchrun): every rank quantizes its own tensors (independent work,
 no collective on the data path); the timing is the max over ranks and `value`
@@ -36,7 +42,6 @@ if ROOT not in sys.path:
 
 METRIC = "dual-axis MXFP8 quantize HBM GB/s (% of GB300 peak); MX9 pack/unpack GB/s"
 DUAL_M, DUAL_N = 65536, 7168
-EVENT_EVERY = 8  # per-kernel events on every 8th timed step (runs of >= 64 steps)
 MX9_ROWS, MX9_COLS = 16384, 8192
 B_DUAL = 4.0625          # bytes per element: 2 in + 1 + 1 + 1/32 + 1/32 out
 B_MX9_F32 = 5.125        # bytes per element: 4 (fp32) + 1 (q) + 1/16 + 1/16
@@ -288,7 +293,114 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def graph_census(g):
+    """Kernel nodes and programmatic (PDL) edges of a captured graph, read with
+    the driver API; None when the graph or the driver entry points are not
+    reachable (the replay-time check below still applies)."""
+    import ctypes
+    try:
+        raw = g.raw_cuda_graph()
+        cu = ctypes.CDLL("libcuda.so.1")
+    except (AttributeError, RuntimeError, OSError):
+        return None
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    n = sz(0)
+    if cu.cuGraphGetNodes(vp(raw), None, ctypes.byref(n)) != 0:
+        return None
+    nodes = (vp * max(n.value, 1))()
+    if cu.cuGraphGetNodes(vp(raw), nodes, ctypes.byref(n)) != 0:
+        return None
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        if cu.cuGraphNodeGetType(vp(nodes[i]), ctypes.byref(t)) != 0:
+            return None
+        kernels += int(t.value == 0)  # CU_GRAPH_NODE_TYPE_KERNEL
+    out = {"nodes": n.value, "kernel_nodes": kernels, "programmatic_edges": None}
+    ne = sz(0)
+    f = getattr(cu, "cuGraphGetEdges_v2", None)
+    if f is not None and f(vp(raw), None, None, None, ctypes.byref(ne)) == 0 and ne.value:
+        frm, to = (vp * ne.value)(), (vp * ne.value)()
+        data = (ctypes.c_uint8 * (8 * ne.value))()  # CUgraphEdgeData: from_port, to_port, type, 5 reserved
+        if f(vp(raw), frm, to, data, ctypes.byref(ne)) == 0:
+            out["programmatic_edges"] = sum(1 for i in range(ne.value) if data[8 * i + 2] != 0)
+    return out
+
+
+def capture_graph(torch, stream, launch):
+    """Capture `launch()` (work enqueued on `stream`) into a CUDA graph; return
+    the graph and its census (graph_census)."""
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        launch()
+    census = graph_census(g)
+    if hasattr(g, "instantiate"):
+        try:
+            g.instantiate()
+        except RuntimeError:
+            pass  # already instantiated at capture end
+    return g, census
+
+
+def upload_graph(g, stream) -> bool:
+    """Upload an instantiated graph to the device ahead of its first replay
+    (driver API cuGraphUpload); False when the handle or entry point is not
+    reachable."""
+    import ctypes
+    try:
+        exe = g.raw_cuda_graph_exec()
+        cu = ctypes.CDLL("libcuda.so.1")
+        return cu.cuGraphUpload(ctypes.c_void_p(exe), ctypes.c_void_p(stream.cuda_stream)) == 0
+    except (AttributeError, RuntimeError, OSError):
+        return False
+
+
+def in_step_breakdown(torch, dev, stream, launches, steps=20, reps=3):
+    """Per-kernel durations inside the graph-replayed step with the
+    programmatic overlap between kernels left intact: a graph of `steps` steps
+    in which every kernel node also feeds an event-record node on a side
+    branch (off the kernel chain), so that each event marks the completion of
+    its kernel.  A kernel's in-step duration is the time from the previous
+    kernel's completion to its own; the first kernel of each replay (timed from
+    the graph's start) is left out.  Returns ({name: [us, ...]}, mean step us)."""
+    side = torch.cuda.Stream(dev)
+    names = [n for n, _ in launches]
+    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in launches] for _ in range(steps)]
+    ev0 = torch.cuda.Event(enable_timing=True, external=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        ev0.record(stream)
+        for k in range(steps):
+            for j, (_, f) in enumerate(launches):
+                f()
+                fork = torch.cuda.Event()
+                fork.record(stream)
+                side.wait_event(fork)
+                ev[k][j].record(side)
+        stream.wait_stream(side)
+    per = {n: [] for n in names}
+    step_us = []
+    for rep in range(reps + 1):
+        g.replay()
+        torch.cuda.synchronize(dev)
+        if rep == 0:
+            continue  # warm replay
+        prev = None
+        for k in range(steps):
+            for j, n in enumerate(names):
+                if prev is not None:
+                    per[n].append(prev.elapsed_time(ev[k][j]) * 1e3)
+                prev = ev[k][j]
+        step_us.append(ev[0][-1].elapsed_time(ev[steps - 1][-1]) * 1e3 / (steps - 1))
+    return per, float(np.mean(step_us))
+
+
 def run_gpu(args):
+    import ctypes
+
     import torch
 
     import mx_block_quantization_gb300 as mxq
@@ -298,7 +410,8 @@ def run_gpu(args):
     rank, world, local = dist_init()
     build_library()
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
+    cap = torch.cuda.Stream(dev)          # the step's kernels are captured on this stream
+    cur = torch.cuda.current_stream(dev)  # graphs replay on the current stream
     seed = rank  # each rank quantizes its own tensors
 
     # ---- inputs (host-generated, seeded) and outputs, resident in HBM
@@ -317,96 +430,121 @@ def run_gpu(args):
     p = torch.empty((nb, 1), dtype=torch.uint8, device=dev)
     y = torch.empty((MX9_ROWS, MX9_COLS), dtype=torch.float32, device=dev)
 
-    # Warm-up goes through the checked Python binding; the timed loop calls the
-    # same C-ABI entry points with pre-marshalled arguments, so host-side
-    # argument handling never leaves the GPU idle between launches.
-    import ctypes
+    # The graph holds the same C-ABI calls as the Python binding makes, with
+    # pre-marshalled arguments; one eager step through the checked binding
+    # first validates every argument.
     L = mxq.lib()
     vp = ctypes.c_void_p
-    hs = vp(stream.cuda_stream)
-    a_dual = (vp(x.data_ptr()), M, N, vp(offs.data_ptr()), offs.numel(),
-              *(vp(t.data_ptr()) for t in dual_out), hs)
-    a_pack = (vp(xm.data_ptr()), mxq.F32, MX9_ROWS, MX9_COLS, vp(q.data_ptr()), vp(e.data_ptr()),
-              vp(p.data_ptr()), hs)
-    a_unpack = (vp(q.data_ptr()), vp(e.data_ptr()), vp(p.data_ptr()), vp(y.data_ptr()), mxq.F32,
-                MX9_ROWS, MX9_COLS, hs)
-    f_dual, f_pack, f_unpack = L.mxq_quantize_2d_dual, L.mx9_pack, L.mx9_unpack
+    hs = vp(cap.cuda_stream)
+    # Step order: the pack, the dual cast, the unpack of the pack's output.  The
+    # three are independent but for the unpack, and this order measured the
+    # fastest whole step: a kernel pays for the dirty L2 lines that its
+    # predecessor leaves, and the dual cast follows the read-heavy pack.
+    kernels = [
+        ("mx9_pack", L.mx9_pack,
+         (vp(xm.data_ptr()), mxq.F32, MX9_ROWS, MX9_COLS, vp(q.data_ptr()), vp(e.data_ptr()),
+          vp(p.data_ptr()), hs)),
+        ("mxq_dual", L.mxq_quantize_2d_dual,
+         (vp(x.data_ptr()), M, N, vp(offs.data_ptr()), offs.numel(), *(vp(t.data_ptr()) for t in dual_out), hs)),
+        ("mx9_unpack", L.mx9_unpack,
+         (vp(q.data_ptr()), vp(e.data_ptr()), vp(p.data_ptr()), vp(y.data_ptr()), mxq.F32,
+          MX9_ROWS, MX9_COLS, hs)),
+    ]
 
-    def step(ev):
-        # ev: four events around the three kernels, or None for an
-        # uninstrumented step (see EVENT_EVERY)
-        if ev is not None:
-            ev[0].record(stream)
-        rc = f_dual(*a_dual)
-        if ev is not None:
-            ev[1].record(stream)
-        rc |= f_pack(*a_pack)
-        if ev is not None:
-            ev[2].record(stream)
-        rc |= f_unpack(*a_unpack)
-        if ev is not None:
-            ev[3].record(stream)
-        if rc:
-            raise mxq.MxqError(rc, "bench step")
+    def launcher(name, fn, a):
+        def launch():
+            rc = fn(*a)
+            if rc:
+                raise mxq.MxqError(rc, name)
+        return launch
 
-    for _ in range(args.warmup):
-        mxq.quantize_2d_dual(x, offs, out=dual_out, stream=stream)
-        mxq.mx9_pack(xm, out=(q, e, p), stream=stream)
-        mxq.mx9_unpack(q, e, p, torch.float32, (MX9_ROWS, MX9_COLS), out=y, stream=stream)
+    launches = [(name, launcher(name, fn, a)) for name, fn, a in kernels]
+
+    def launch_step():
+        for _, f in launches:
+            f()
+
+    with torch.cuda.stream(cap):
+        mxq.mx9_pack(xm, out=(q, e, p), stream=cap)
+        mxq.quantize_2d_dual(x, offs, out=dual_out, stream=cap)
+        mxq.mx9_unpack(q, e, p, torch.float32, (MX9_ROWS, MX9_COLS), out=y, stream=cap)
     torch.cuda.synchronize(dev)
-    assert mxq.device_status(clear=True) == 0
+    # the warm-up replays a one-step graph; the timed region replays, once, a
+    # graph of the K steps, so that consecutive steps also follow each other
+    # with programmatic dependent launch
+    step_graph, census1 = capture_graph(torch, cap, launch_step)
 
-    # per-kernel events on every EVENT_EVERY-th step of the timed region: an
-    # event between two kernels costs the step ~1.6% (measured), which the
-    # sampled steps still pay but the others do not
-    every = EVENT_EVERY if args.steps >= 8 * EVENT_EVERY else 1  # short runs: every step
-    evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-           for k in range(0, args.steps, every)}
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    def launch_k_steps():
+        for _ in range(args.steps):
+            launch_step()
+
+    timed_graph, census = capture_graph(torch, cap, launch_k_steps)
+    for c, k in ((census1, 1), (census, args.steps)):
+        if c is not None:
+            assert c["kernel_nodes"] == len(launches) * k, f"graph of {k} steps: {c}"
+
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)  # let the sampler start before the timed region
-    barrier(world)
+    for _ in range(args.warmup):
+        step_graph.replay()
+    uploaded = upload_graph(timed_graph, cur)  # so that the timed replay does not pay for it
     torch.cuda.synchronize(dev)
-    t_start.record(stream)
-    for k in range(args.steps):
-        step(evs.get(k))
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clocks = sampler.stop()
     assert mxq.device_status(clear=True) == 0
 
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
-    value = aggregate_gbs(sum(step_bytes().values()), args.steps, world, total_ms)
-    per = {"mxq_dual": [], "mx9_pack": [], "mx9_unpack": []}
-    for ev in evs.values():
-        per["mxq_dual"].append(ev[0].elapsed_time(ev[1]))
-        per["mx9_pack"].append(ev[1].elapsed_time(ev[2]))
-        per["mx9_unpack"].append(ev[2].elapsed_time(ev[3]))
+    # ---- timed region: the K-step graph, no events inside
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(cur)
+    timed_graph.replay()
+    t_end.record(cur)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    assert mxq.device_status(clear=True) == 0
     sb = step_bytes()
     bytes_per_step = sum(sb.values())
-    ms_per_step = total_ms / args.steps
+    own_ms = t_start.elapsed_time(t_end)
     peak, peak_kind = measured_peak()
+    # a replay that did no work would be far faster than the copy rate allows
+    assert own_ms > 0.5 * args.steps * bytes_per_step / (peak * 1e9) * 1e3, "empty step graph"
+    total_ms = max_over_ranks(own_ms, world)
+    value = aggregate_gbs(bytes_per_step, args.steps, world, total_ms)
+    ms_per_step = total_ms / args.steps
+
+    # ---- per-kernel figures, from separate passes after the timed region
+    per, step_us_inst = in_step_breakdown(torch, dev, cap, launches)
     breakdown = {}
-    for k, v in per.items():
-        avg = float(np.mean(v))
-        gbs = sb[k] / (avg / 1e3) / 1e9
-        breakdown[k] = {"avg_us": avg * 1e3, "gbs": gbs, "frac_of_measured": gbs / peak,
-                        "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                        "algorithmic_bytes": sb[k]}
-    dual_avg_s = float(np.mean(per["mxq_dual"])) / 1e3
-    achieved = sb["mxq_dual"] / dual_avg_s / 1e9
-    traffic = profiled_traffic()
+    for name, f in launches:
+        avg = float(np.mean(per[name]))
+        gbs = sb[name] / (avg / 1e6) / 1e9
+        iso = graph_time(torch, dev, lambda s, f=f: f(), per_graph=20, replays=5, stream=cap)
+        iso_gbs = sb[name] / (iso / 1e6) / 1e9
+        breakdown[name] = {"avg_us": avg, "gbs": gbs, "frac_of_measured": gbs / peak,
+                           "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                           "algorithmic_bytes": sb[name],
+                           "isolated": {"us": iso, "gbs": iso_gbs, "frac_of_measured": iso_gbs / peak}}
+    clocks = sampler.stop()
+    assert mxq.device_status(clear=True) == 0
+    achieved = breakdown["mxq_dual"]["gbs"]
     roofline = {"bound": "hbm", "kernel": "mxq_tile_kernel<kDual>", "achieved": achieved, "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "algorithmic_bytes": sb["mxq_dual"],
-                "timing": f"CUDA events around each kernel on every {every}th timed step "
-                          f"({len(evs)} of {args.steps})"}
+                "traffic": profiled_traffic(), "algorithmic_bytes": sb["mxq_dual"],
+                "timing": ("in-step duration (previous kernel's completion to this one's) from CUDA "
+                           "events recorded by side-branch nodes of a 20-step graph of the same step, "
+                           "replayed 3 times after the timed region; the programmatic overlap between "
+                           "kernels is kept")}
+    graph_info = {"steps_per_graph": args.steps, "replays_timed": 1, "uploaded_before_timing": uploaded,
+                  "kernel_nodes": None if census is None else census["kernel_nodes"],
+                  "programmatic_edges": None if census is None else census["programmatic_edges"],
+                  "instrumented_step_us": step_us_inst}
+
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = measure_configs(mxq, torch, dev, peak)
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, mxq, torch, dev, stream, xd_h, offs, xm_h, dual_out, (q, e, p), y, world)
+    e2e = run_e2e(args, mxq, torch, dev, cur, xd_h, offs, xm_h, dual_out, (q, e, p), y, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -419,9 +557,13 @@ def run_gpu(args):
                 "dtype": "f32", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                            "l2": "inputs larger than L2 (129 MB); no flush",
+                           "timing": "one replay of a CUDA graph holding the K steps (3 kernel "
+                                     "nodes each, programmatic dependent launch between them), "
+                                     "one event pair around it",
                            "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 3 * args.steps, "clocks": clocks, "breakdown": breakdown}
+                "gpu_launches": len(launches) * args.steps, "clocks": clocks,
+                "graph": graph_info, "breakdown": breakdown, "configs": configs}
         print(json.dumps(line), flush=True)
     if args.sweep:
         run_sweep(mxq, torch, dev, rank)
@@ -429,6 +571,103 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _dual_outputs(mxq, torch, dev, M, N):
+    kw = dict(dtype=torch.uint8, device=dev)
+    return mxq.DualOutputs(torch.empty((M, N), **kw), torch.empty((M * N // 32,), **kw),
+                           torch.empty((N, M), **kw), torch.empty((M * N // 32,), **kw))
+
+
+def measure_configs(mxq, torch, dev, peak):
+    """Graph-replay throughput of every workload besides the step's (20
+    launches per graph, median of 5 replays): the 128x128 case, the MX9
+    4096x4096 outlier tensor, the 8192x8192 specials tensor, the throughput
+    sweep (fused cast, its three-pass composition and the speedup, MX9 fp32
+    and bf16) and the packed MX9/MX6 tensor along both axes at 16384x8192."""
+    from mx_block_quantization_gb300 import workloads as W
+
+    def rate(us, nbytes):
+        gbs = nbytes / (us / 1e6) / 1e9
+        return {"us": round(us, 3), "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4)}
+
+    def t(launch):
+        return graph_time(torch, dev, launch, per_graph=20, replays=5)
+
+    def bf16_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    res = {"peak_gbs": peak, "timing": "CUDA-graph replay, 20 launches per graph, median of 5"}
+    xb, offs1 = W.dual_small()
+    x, o = bf16_dev(xb), torch.from_numpy(offs1).to(dev)
+    out = _dual_outputs(mxq, torch, dev, 128, 128)
+    res["dual_128x128_one_group"] = {
+        **rate(t(lambda s: mxq.quantize_2d_dual(x, o, out=out, stream=s)), B_DUAL * 128 * 128),
+        "note": "66.6 KB per launch: launch-bound, L2-resident"}
+    xf = torch.from_numpy(W.mx9_outliers()).to(dev)
+    for dt, tdt, bpe in (("f32", torch.float32, B_MX9_F32), ("bf16", torch.bfloat16, 3.125)):
+        xin = xf.to(tdt)
+        q, e, p = mxq.mx9_pack(xin)
+        yy = torch.empty_like(xin)
+        nbytes = bpe * xin.numel()
+        res[f"mx9_outliers_4096x4096_{dt}"] = {
+            "pack": rate(t(lambda s: mxq.mx9_pack(xin, out=(q, e, p), stream=s)), nbytes),
+            "unpack": rate(t(lambda s: mxq.mx9_unpack(q, e, p, tdt, tuple(xin.shape), out=yy, stream=s)),
+                           nbytes),
+            "l2_resident": nbytes < 129e6}
+    del xf, xin, q, e, p, yy
+    xs = bf16_dev(W.dual_specials())
+    out = _dual_outputs(mxq, torch, dev, 8192, 8192)
+    res["dual_specials_8192x8192_dense"] = rate(t(lambda s: mxq.quantize_2d_dual(xs, out=out, stream=s)),
+                                                B_DUAL * 8192 * 8192)
+    del xs, out
+    sweep, speedups = {}, []
+    gen = torch.Generator(device=dev)
+    for (M, N) in W.SWEEP_SHAPES:
+        gen.manual_seed(0)
+        xf = torch.randn((M, N), generator=gen, device=dev, dtype=torch.float32)
+        xb16 = xf.to(torch.bfloat16)
+        out = _dual_outputs(mxq, torch, dev, M, N)
+        ws = torch.empty((M * N // 32,), dtype=torch.uint8, device=dev)
+        fused = t(lambda s: mxq.quantize_2d_dual(xb16, out=out, stream=s))
+        three = t(lambda s: mxq.quantize_2d_dual_3pass(xb16, workspace=ws, out=out, stream=s))
+        row = {"dual": rate(fused, B_DUAL * M * N), "dual_3pass": rate(three, B_DUAL * M * N),
+               "fused_speedup_vs_3pass": round(three / fused, 3),
+               "l2_resident": B_DUAL * M * N < 129e6}
+        speedups.append(three / fused)
+        del out, ws
+        for dt, xin, bpe in (("f32", xf, B_MX9_F32), ("bf16", xb16, 3.125)):
+            q, e, p = mxq.mx9_pack(xin)
+            yy = torch.empty_like(xin)
+            row[f"mx9_pack_{dt}"] = rate(t(lambda s: mxq.mx9_pack(xin, out=(q, e, p), stream=s)), bpe * M * N)
+            row[f"mx9_unpack_{dt}"] = rate(t(lambda s: mxq.mx9_unpack(
+                q, e, p, xin.dtype, (M, N), out=yy, stream=s)), bpe * M * N)
+            del q, e, p, yy
+        sweep[f"{M}x{N}"] = row
+        del xf, xb16
+        torch.cuda.empty_cache()
+    res["sweep"] = sweep
+    res["fused_speedup_geomean"] = round(float(np.exp(np.mean(np.log(speedups)))), 3)
+    res["fused_speedup_pages"] = "2.6x geomean, 2.0x at the largest shape (GB200, 2062 MHz)"
+    M, N = 16384, 8192
+    gen.manual_seed(1)
+    xf = torch.randn((M, N), generator=gen, device=dev, dtype=torch.float32)
+    packed = {}
+    for dt, xin, esz in (("f32", xf, 4), ("bf16", xf.to(torch.bfloat16), 2)):
+        yy = torch.empty_like(xin)
+        for fmt, fname in ((mxq.FMT_MX9, "mx9"), (mxq.FMT_MX6, "mx6")):
+            nbytes = (esz + mxq.RECORD_BYTES[fmt] / 16) * M * N
+            for axis, aname in ((1, "rows"), (0, "cols")):
+                rec = mxq.mx_pack_packed(xin, fmt, axis)
+                packed[f"{fname}_{aname}_{dt}"] = {
+                    "pack": rate(t(lambda s: mxq.mx_pack_packed(xin, fmt, axis, out=rec, stream=s)), nbytes),
+                    "unpack": rate(t(lambda s: mxq.mx_unpack_packed(rec, fmt, yy, axis, stream=s)), nbytes)}
+                del rec
+        del yy
+    res[f"packed_{M}x{N}"] = packed
+    del xf
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(args, mxq, torch, dev, stream, xd_h, offs, xm_h, dual_out, mx9_parts, y, world):
@@ -472,8 +711,8 @@ def run_e2e(args, mxq, torch, dev, stream, xd_h, offs, xm_h, dual_out, mx9_parts
         if k >= 2:
             s_comp.wait_event(sl["d2h_done"])         # outputs of step k-2 downloaded
         q, e, p = sl["mx9"]
-        mxq.quantize_2d_dual(sl["x"], offs, out=sl["dual"], stream=s_comp)
         mxq.mx9_pack(sl["xm"], out=(q, e, p), stream=s_comp)
+        mxq.quantize_2d_dual(sl["x"], offs, out=sl["dual"], stream=s_comp)
         mxq.mx9_unpack(q, e, p, torch.float32, tuple(sl["xm"].shape), out=sl["y"], stream=s_comp)
         sl["comp_done"].record(s_comp)
         with torch.cuda.stream(s_d2h):
@@ -507,66 +746,12 @@ def run_e2e(args, mxq, torch, dev, stream, xd_h, offs, xm_h, dual_out, mx9_parts
 
 
 def run_sweep(mxq, torch, dev, rank):
-    """Throughput sweep shapes under CUDA-graph replay (20 launches per graph)."""
-    from mx_block_quantization_gb300 import workloads as W
+    """With --sweep: the packed tensor in its other geometries (blocks along
+    columns, and blocked rows at a pitch of cols + 64, the input a strided
+    view) at a mid and a large shape, one line each, under graph replay."""
     peak, kind = measured_peak()
-    speedups = []
-    for (M, N) in W.SWEEP_SHAPES:
-        res = {}
-        x = torch.from_numpy(W.normal_bf16((M, N), seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
-        kw = dict(dtype=torch.uint8, device=dev)
-        out = mxq.DualOutputs(torch.empty((M, N), **kw), torch.empty((M * N // 32,), **kw),
-                              torch.empty((N, M), **kw), torch.empty((M * N // 32,), **kw))
-        res["mxq_dual"] = (graph_time(torch, dev, lambda s: mxq.quantize_2d_dual(x, out=out, stream=s)),
-                           B_DUAL * M * N)
-        # the three-pass composition the fused cast replaces (same outputs, two reads of x)
-        ws = torch.empty((M * N // 32,), **kw)
-        res["mxq_dual_3pass"] = (graph_time(torch, dev, lambda s: mxq.quantize_2d_dual_3pass(
-            x, workspace=ws, out=out, stream=s)), B_DUAL * M * N)
-        del x, out, ws
-        for dt, tdt, bpe in (("f32", torch.float32, B_MX9_F32), ("bf16", torch.bfloat16, 3.125)):
-            xm = torch.from_numpy(W.normal_f32((M, N), seed=0)).to(dev).to(tdt)
-            q, e, p = mxq.mx9_pack(xm)
-            yy = torch.empty_like(xm)
-            res[f"mx9_pack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx9_pack(xm, out=(q, e, p), stream=s)),
-                                     bpe * M * N)
-            res[f"mx9_unpack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx9_unpack(
-                q, e, p, tdt, (M, N), out=yy, stream=s)), bpe * M * N)
-            # the single packed tensor (MX9 18-byte and MX6 12-byte records, blocks along rows)
-            esz = 4 if dt == "f32" else 2
-            for fmt, name in ((mxq.FMT_MX9, "mx9"), (mxq.FMT_MX6, "mx6")):
-                rec = mxq.mx_pack_packed(xm, fmt, 1)
-                pbytes = (esz + mxq.RECORD_BYTES[fmt] / 16) * M * N
-                res[f"{name}_packed_pack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx_pack_packed(
-                    xm, fmt, 1, out=rec, stream=s)), pbytes)
-                res[f"{name}_packed_unpack_{dt}"] = (graph_time(torch, dev, lambda s: mxq.mx_unpack_packed(
-                    rec, fmt, yy, 1, stream=s)), pbytes)
-                del rec
-            del xm, q, e, p, yy
-        if rank == 0:
-            line = {"sweep_shape": [M, N], "peak_gbs": peak, "peak_kind": kind,
-                    "l2_resident": (B_DUAL * M * N) < 129e6}
-            for k, (us, b) in res.items():
-                gbs = b / (us / 1e6) / 1e9
-                line[k] = {"us": us, "gbs": gbs, "frac_of_measured": gbs / peak,
-                           "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
-            speedup = res["mxq_dual_3pass"][0] / res["mxq_dual"][0]
-            line["fused_speedup_vs_3pass"] = speedup
-            speedups.append(speedup)
-            print(json.dumps(line), flush=True)
-        torch.cuda.empty_cache()
-    # the packed tensor in its other geometries: blocks along columns, and
-    # blocked rows at a pitch of cols + 64 (the input a strided view), at a
-    # mid and a large shape
     for M, N in ((16384, 8192), (32768, 16384)):
         run_sweep_packed(mxq, torch, dev, rank, M, N, peak, kind)
-    if rank == 0:
-        geo = float(np.exp(np.mean(np.log(speedups))))
-        print(json.dumps({"sweep_summary": "fused dual-axis cast vs three-pass composition, "
-                          "CUDA-graph replay", "geomean_speedup": geo,
-                          "largest_shape_speedup": speedups[-1],
-                          "pages_figures": "2.6x geomean, 2.0x largest (GB200, 2062 MHz)"}),
-              flush=True)
 
 
 def run_sweep_packed(mxq, torch, dev, rank, M, N, peak, kind):
@@ -593,10 +778,10 @@ def run_sweep_packed(mxq, torch, dev, rank, M, N, peak, kind):
     torch.cuda.empty_cache()
 
 
-def graph_time(torch, dev, launch, per_graph=20, replays=10):
-    """Median per-launch time (us) of `launch` captured per_graph times into one
-    CUDA graph; the graph must contain kernel work (timed replay > 0)."""
-    s = torch.cuda.Stream(dev)
+def graph_time(torch, dev, launch, per_graph=20, replays=10, stream=None):
+    """Median per-launch time (us) of `launch(stream)` captured per_graph times
+    into one CUDA graph; the graph must contain kernel work (timed replay > 0)."""
+    s = torch.cuda.Stream(dev) if stream is None else stream
     with torch.cuda.stream(s):
         launch(s)
     torch.cuda.synchronize(dev)
@@ -684,8 +869,10 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload graph-replay figures of the JSON line's configs key")
     ap.add_argument("--sweep", action="store_true",
-                    help="also print one line per throughput-sweep shape (graph replay)")
+                    help="also print one line per packed-tensor geometry (graph replay)")
     ap.add_argument("--case", choices=["dual", "dual3", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16",
                                        "rec_pack_f32", "rec_pack_bf16", "rec_unpack_f32",
                                        "rec_unpack_bf16"],

@@ -6,7 +6,10 @@
  * library never allocates, never frees and never synchronizes inside these
  * calls.  Work is enqueued on the caller's `stream` (0 = legacy default
  * stream), so every call can be captured in a CUDA graph and ordered with the
- * caller's own work.
+ * caller's own work.  Kernels are launched with programmatic dependent launch:
+ * one may be scheduled, and run its shared-memory set-up, while the previous
+ * kernel on the stream is still running, but it touches no global memory
+ * before that kernel has completed, so stream order is kept exactly.
  *
  * Return value: MXQ_OK (0) when the work was enqueued, a negative MXQ_E* code
  * when an argument was rejected (nothing is enqueued and no byte of any output
@@ -69,8 +72,9 @@ typedef struct CUstream_st *cudaStream_t;
  * zeroed for the uncovered tail past offs[G-1].
  *
  *   x      bf16 [M, N] row-major (2*M*N bytes), 16-byte aligned.
- *   M, N   multiples of 128, >= 0 ([AO]: "both dimensions and every group size
- *          must be multiples of 128").  M == 0 or N == 0 is a no-op.
+ *   M, N   multiples of 128, >= 0 (the [AO] description requires both sizes and
+ *          every group size to be multiples of 128).  M == 0 or N == 0 is a
+ *          no-op.
  *   offs   device int32 [G]: cumulative group ends, non-decreasing, each a
  *          multiple of 128, offs[G-1] <= M (empty groups allowed); 4-byte
  *          aligned.  NULL selects dense placement (one group [0, M)); then G
@@ -162,10 +166,9 @@ int mx9_unpack(const int8_t *q, const uint8_t *max_exp, const uint8_t *prime, vo
                int64_t rows, int64_t cols, cudaStream_t stream);
 
 /*
- * MX9 and MX6 in one packed uint8 tensor ([MX9] commits "pack mx9 into a
- * single uint8 tensor and dispatch mx6/mx9 to the packed kernels" and
- * "consume strided quantization inputs"; the suite's axis, non-contiguous and
- * padding tests).  One record per 16-element block, [exponent byte, prime
+ * MX9 and MX6 in one packed uint8 tensor ([MX9] commits: MX9 packed into one
+ * uint8 tensor with MX6 and MX9 sent to the packed kernels, and strided inputs
+ * accepted; the suite's axis, non-contiguous and padding tests).  One record per 16-element block, [exponent byte, prime
  * byte, data] (the review excerpt stores the exponent at the record start):
  *   MXQ_FMT_MX9: data = 16 int8 q as in mx9_pack; 18-byte records, 9 bits/elem.
  *   MXQ_FMT_MX6: the same rule with 4 magnitude bits, k = max(E - 3 - prime,
@@ -245,7 +248,10 @@ int mxq_quantize_2d_dual_3pass(const void *x, int64_t M, int64_t N, const int32_
  *   workspace; returns MXQ_ESCRATCH, enqueuing nothing, when M*N/32 exceeds
  *   MXQ_NOALLOC_SCRATCH_BYTES (16 MiB: M*N up to 2^29 elements).
  *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   device current; make that first call before any stream capture.  The
+ *   address is looked up again when the current context changes (after a
+ *   device reset, say), so the first call in a new context also belongs
+ *   before any capture.
  *   All calls share the one array and each overwrites the part it uses before
  *   reading it: calls that may overlap on the GPU (different streams without
  *   ordering between them) race on it and must be serialized by the caller.
@@ -261,8 +267,13 @@ int mxq_quantize_2d_dual_3pass_noalloc(const void *x, int64_t M, int64_t N, cons
  * `clear` is non-zero.  This call synchronizes the device (it reads device
  * memory); use it for diagnostics and tests, not inside captured work.
  * Returns MXQ_OK, MXQ_ENULL or MXQ_ECUDA.
+ * mxq_last_device_status is the same call under the boundary's other name: the
+ * word lives in device memory and is read by a copy (hence the synchronization)
+ * instead of in a library-owned pinned host flag, so that no compute call
+ * needs an allocation.
  */
 int mxq_device_status(uint32_t *out, int clear);
+int mxq_last_device_status(uint32_t *out, int clear);
 
 /*
  * Self-test of failure detection, on the GPU and without a fault: launches one

@@ -20,9 +20,10 @@
 // The same kernel writes the packed MX9 / MX6 record forms of mx_packed.cu
 // (blocked rows read at a pitch: one bulk copy per row piece of a stage),
 // staging each warp's 32 records and storing them with one bulk copy.
-// unpack: a streaming kernel, one wave of resident blocks; each lane writes 16
-// output bytes (4 fp32 or 8 bf16 elements), exact q * 2^k built without
-// conversion instructions.
+// unpack: a streaming kernel, one wave of resident blocks; each lane decodes
+// whole 16-element blocks (exact q * 2^k built without conversion
+// instructions) and a per-warp shared-memory transpose turns them into
+// 512-byte contiguous stores.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -88,6 +89,16 @@ using namespace mxq;
 #endif
 #ifndef MXQ_MX9_UNPACK_UNROLL_BF16
 #define MXQ_MX9_UNPACK_UNROLL_BF16 4
+#endif
+
+// Unpack round order: 1 = each warp takes kUnroll adjacent rounds of 32
+// blocks, 2 = grid-wide rounds (round u of all warps adjacent, so the grid
+// writes one contiguous stretch at a time).  2 measured best inside the bench
+// step; a former kernel with a lane per 16 output bytes (four lanes sharing a
+// block, each loading its exponent and prime bytes) was 3% faster back to
+// back but 1-2% slower in the step, after the pack or the dual cast.
+#ifndef MXQ_MX9_UNPACK_KIND
+#define MXQ_MX9_UNPACK_KIND 2
 #endif
 
 constexpr int kUnpackBlock = 256;
@@ -178,6 +189,8 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
     mbar_init_fence();
   }
   __syncthreads();
+  pdl_wait();  // x may be the previous kernel's output; outputs may still be read by it
+  pdl_trigger_at_start();
 
   if (warp == S::kWarps) {
     // ------------------------------------------------------------ producer
@@ -216,6 +229,7 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
       }
       issued = i + 1;
     }
+    pdl_trigger_at_end();
     // drain (a no-op after a normal run: consumers waited for every stage)
     for (int64_t i = issued > S::kStages ? issued - S::kStages : 0; i < issued; ++i)
       mbar_wait_drain(full(static_cast<int>(i % S::kStages)),
@@ -308,6 +322,7 @@ __global__ void __launch_bounds__(PackShape<kBF16, kOut>::kThreads, MXQ_MX9_PACK
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(s));
   }
+  pdl_trigger_at_end();
   if (kOut != kSplit && lane == 0) bulk_wait_all<0>();
 }
 
@@ -332,16 +347,33 @@ __device__ __forceinline__ float small_int_to_float(int32_t q) {
   return fadd_rn_noftz(__int_as_float(0x4B400000 + q), -12582912.0f);
 }
 
-// A lane writes 16 output bytes: 4 fp32 or 8 bf16 elements, so 4 (fp32) or
-// 2 (bf16) lanes share a block.  q * 2^k is exact (|q| <= 127, k >= -126)
-// except for overflow in max_exp 255 blocks; a bf16 result has at most 7
-// significant bits, so the top half of the fp32 is the exact bf16.
+// Unpack: a lane decodes whole 16-element blocks, one per round: one 16-byte
+// load of q plus the block's own exponent and prime bytes (a warp's loads of a
+// round are 512 contiguous q bytes and 32 contiguous bytes of each of the
+// others), kUnroll rounds' loads issued before the first decode.  The decoded
+// block (64 bytes of fp32 or 32 of bf16) goes to a per-warp staging buffer in
+// shared memory, from which each lane stores 16-byte pieces so that every
+// store instruction writes 512 contiguous output bytes.  q * 2^k is exact
+// (|q| <= 127, k >= -126) except for overflow in max_exp 255 blocks; a bf16
+// result has at most 7 significant bits, so the top half of the fp32 is the
+// exact bf16.
 template <bool kBF16>
-struct UnpackLane {
-  static constexpr int kElems = kBF16 ? 8 : 4;
-  static constexpr int kLanesPerBlock = 16 / kElems;
+struct UnpackShape {
+  static constexpr int kChunks = kBF16 ? 2 : 4;  // 16-byte output pieces per block
   static constexpr int kUnroll = kBF16 ? MXQ_MX9_UNPACK_UNROLL_BF16 : MXQ_MX9_UNPACK_UNROLL_F32;
+  static constexpr int kWarps = kUnpackBlock / 32;
+  static constexpr int kGroup = 32 * kUnroll;                   // blocks per warp iteration
+  static constexpr uint32_t kStageBytes = 32u * kChunks * 16u;  // one round of a warp
 };
+
+// Slot of output piece c (piece c % kChunks of the round's block c / kChunks)
+// in a warp's staging buffer.  XOR-ing bits 3.. of c into its low bits makes
+// both access patterns conflict-free: the writes, where lane l stores the
+// pieces of its own block, and the reads, where lane l loads piece 32r + l.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t unpack_slot(int c) {
+  return static_cast<uint32_t>(kBF16 ? c ^ ((c >> 3) & 1) : c ^ ((c >> 3) & 3));
+}
 
 __device__ __forceinline__ void unpack4(uint32_t w, float s0, float s1, float* y) {
   const int32_t v = static_cast<int32_t>(w);
@@ -366,90 +398,101 @@ __device__ __forceinline__ void unpack4_biased(uint32_t vx, float s0, float s1, 
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
-    const uint32_t* __restrict__ q, const uint8_t* __restrict__ max_exp,
-    const uint8_t* __restrict__ prime, void* __restrict__ y, int64_t nchunks) {
-  using U = UnpackLane<kBF16>;
-  const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kUnpackBlock;
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kUnpackBlock + (threadIdx.x - lane);
-  // pairs handled by this lane inside its block, and their prime-bit shift
-  const int pshift = (lane % U::kLanesPerBlock) * (U::kElems / 2);
-  for (int64_t base = warp0; base < nchunks; base += stride * U::kUnroll) {
-    uint32_t qv[U::kUnroll][U::kElems / 4], ev[U::kUnroll], pv[U::kUnroll];
+    const uint4* __restrict__ q, const uint8_t* __restrict__ max_exp,
+    const uint8_t* __restrict__ prime, uint4* __restrict__ y, int64_t nb) {
+  using U = UnpackShape<kBF16>;
+  __shared__ __align__(16) uint8_t stage[U::kWarps][U::kStageBytes];
+  pdl_wait();
+  pdl_trigger_at_start();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t st = smem_u32(stage[warp]);
+  const int64_t gwarps = static_cast<int64_t>(gridDim.x) * U::kWarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * U::kWarps + warp;
+  // first block of round u of iteration it: a warp's own group of kUnroll
+  // rounds, or grid-wide rounds (all warps' round u adjacent)
+  auto round_base = [&](int64_t it, int u) -> int64_t {
+    return MXQ_MX9_UNPACK_KIND == 2 ? ((it * U::kUnroll + u) * gwarps + gw) * 32
+                                    : (it * gwarps + gw) * U::kGroup + 32 * u;
+  };
+  for (int64_t it = 0; round_base(it, 0) < nb; ++it) {
+    uint4 qv[U::kUnroll];
+    uint32_t ev[U::kUnroll], pv[U::kUnroll];
 #pragma unroll
     for (int u = 0; u < U::kUnroll; ++u) {
-      const int64_t c = base + u * stride + lane;
-      if (c < nchunks) {
-        // q: nchunks * kElems bytes; exponent and prime bytes: one per block
-        const uint64_t nblk = static_cast<uint64_t>(nchunks) / U::kLanesPerBlock;
-        if (in_buf(reinterpret_cast<const uint8_t*>(q) + U::kElems * c, U::kElems, q,
-                   static_cast<uint64_t>(nchunks) * U::kElems, &g_mx9_status) &&
-            in_buf(max_exp + c / U::kLanesPerBlock, 1, max_exp, nblk, &g_mx9_status) &&
-            in_buf(prime + c / U::kLanesPerBlock, 1, prime, nblk, &g_mx9_status)) {
-          if (kBF16) {
-            const uint2 w = __ldcs(reinterpret_cast<const uint2*>(q) + c);
-            qv[u][0] = w.x;
-            qv[u][U::kElems / 4 - 1] = w.y;
-          } else {
-            qv[u][0] = __ldcs(q + c);
-          }
-          ev[u] = __ldg(max_exp + c / U::kLanesPerBlock);
-          pv[u] = __ldg(prime + c / U::kLanesPerBlock);
-        } else {
-          qv[u][0] = qv[u][U::kElems / 4 - 1] = ev[u] = pv[u] = 0;
-        }
-      } else {
-        qv[u][0] = qv[u][U::kElems / 4 - 1] = ev[u] = pv[u] = 0;
+      const int64_t b = round_base(it, u) + lane;
+      qv[u] = make_uint4(0u, 0u, 0u, 0u);
+      ev[u] = pv[u] = 0u;
+      if (b < nb && in_buf(q + b, 16, q, 16ull * nb, &g_mx9_status) &&
+          in_buf(max_exp + b, 1, max_exp, nb, &g_mx9_status) &&
+          in_buf(prime + b, 1, prime, nb, &g_mx9_status)) {
+        qv[u] = __ldcs(q + b);
+        ev[u] = __ldg(max_exp + b);
+        pv[u] = __ldg(prime + b);
       }
     }
 #pragma unroll
     for (int u = 0; u < U::kUnroll; ++u) {
-      const int64_t c = base + u * stride + lane;
-      if (c >= nchunks) continue;
+      const int64_t bu = round_base(it, u);  // first block of the round (warp-uniform)
+      if (bu >= nb) break;
       const int E = static_cast<int>(ev[u]) - 127;
-      const int pbits = static_cast<int>(pv[u] >> pshift);
-      float s[U::kElems / 2];
-      float v[U::kElems];
+      const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+      float v[16];  // word k holds elements 4k..4k+3, i.e. pairs 2k and 2k+1
       if (kBF16 ? MXQ_MX9_UNPACK_PRMT_BF16 : MXQ_MX9_UNPACK_PRMT_F32) {
         // the two possible pair scales, then one select per pair
         const float s_keep = exp2_normal(max(E - 6, -126)), s_dem = exp2_normal(max(E - 7, -126));
 #pragma unroll
-        for (int k = 0; k < U::kElems / 2; ++k) s[k] = (pbits >> k) & 1 ? s_dem : s_keep;
-#pragma unroll
-        for (int k = 0; k < U::kElems / 4; ++k)
-          unpack4_biased(qv[u][k] ^ 0x80808080u, s[2 * k], s[2 * k + 1], v + 4 * k);
+        for (int k = 0; k < 4; ++k)
+          unpack4_biased(w[k] ^ 0x80808080u, (pv[u] >> (2 * k)) & 1u ? s_dem : s_keep,
+                         (pv[u] >> (2 * k + 1)) & 1u ? s_dem : s_keep, v + 4 * k);
       } else {
 #pragma unroll
-        for (int k = 0; k < U::kElems / 2; ++k)
-          s[k] = exp2_normal(max(E - 6 - ((pbits >> k) & 1), -126));
-#pragma unroll
-        for (int k = 0; k < U::kElems / 4; ++k) unpack4(qv[u][k], s[2 * k], s[2 * k + 1], v + 4 * k);
+        for (int k = 0; k < 4; ++k)
+          unpack4(w[k], exp2_normal(max(E - 6 - static_cast<int>((pv[u] >> (2 * k)) & 1u), -126)),
+                  exp2_normal(max(E - 6 - static_cast<int>((pv[u] >> (2 * k + 1)) & 1u), -126)),
+                  v + 4 * k);
       }
-      if (!in_buf(reinterpret_cast<uint8_t*>(y) + 16 * c, 16, y, 16ull * nchunks, &g_mx9_status)) {
-        continue;
-      } else if (kBF16) {
-        uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // the high halves of two fp32 values
-          o[k] = __byte_perm(__float_as_uint(v[2 * k]), __float_as_uint(v[2 * k + 1]), 0x7632);
-        __stcs(reinterpret_cast<uint4*>(y) + c, make_uint4(o[0], o[1], o[2], o[3]));
-      } else {
-        __stcs(reinterpret_cast<float4*>(y) + c, make_float4(v[0], v[1], v[2], v[3]));
+      for (int j = 0; j < U::kChunks; ++j) {
+        const uint32_t a = st + 16u * unpack_slot<kBF16>(U::kChunks * lane + j);
+        if (kBF16) {  // the high halves of fp32 pairs
+          const float* h = v + 8 * j;
+          sts128(a, __byte_perm(__float_as_uint(h[0]), __float_as_uint(h[1]), 0x7632),
+                 __byte_perm(__float_as_uint(h[2]), __float_as_uint(h[3]), 0x7632),
+                 __byte_perm(__float_as_uint(h[4]), __float_as_uint(h[5]), 0x7632),
+                 __byte_perm(__float_as_uint(h[6]), __float_as_uint(h[7]), 0x7632));
+        } else {
+          sts128(a, __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                 __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+        }
       }
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < U::kChunks; ++r) {
+        const int c = 32 * r + lane;
+        const uint4 o = lds128(st + 16u * unpack_slot<kBF16>(c));
+        const int64_t piece = bu * U::kChunks + c;
+        if (bu + c / U::kChunks < nb &&
+            in_buf(y + piece, 16, y, 16ull * U::kChunks * nb, &g_mx9_status))
+          __stcs(y + piece, o);
+      }
+      __syncwarp();  // the buffer is rewritten by the next round
     }
   }
+  pdl_trigger_at_end();
 }
 
 // One full wave: as many resident blocks as the kernel's occupancy allows on
-// every SM, or fewer when the problem is small.
+// every SM, or fewer when the problem is small (one warp per group of
+// `group` 16-element blocks).
 template <typename Kernel>
-unsigned unpack_grid(Kernel kernel, int64_t nchunks, int sms) {
+unsigned unpack_grid(Kernel kernel, int64_t nb, int group, int sms) {
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kUnpackBlock, 0) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int64_t want = (nchunks + kUnpackBlock - 1) / kUnpackBlock;
+  const int64_t warps = (nb + group - 1) / group;
+  const int64_t want = (warps + kUnpackBlock / 32 - 1) / (kUnpackBlock / 32);
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<unsigned>(want < cap ? want : cap);
 }
@@ -480,6 +523,8 @@ cudaError_t launch_pack(const void* x, int64_t nb, int64_t nbl, int64_t pitch, u
   cfg.blockDim = dim3(S::kThreads);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
   return cudaLaunchKernelEx(&cfg, mx9_pack_kernel<kBF16, kOut>, static_cast<const uint8_t*>(x),
                             nb, nbl, pitch, q_or_rec, max_exp, prime);
 }
@@ -563,16 +608,20 @@ extern "C" int mx9_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
   const int sms = sm_count_current_device(nullptr);
   if (sms <= 0) return MXQ_ECUDA;
 
-  const int64_t nchunks = n / (dtype == MXQ_F32 ? UnpackLane<false>::kElems : UnpackLane<true>::kElems);
+  const int64_t nb = n / 16;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(dtype == MXQ_F32 ? unpack_grid(mx9_unpack_kernel<false>, nchunks, sms)
-                                      : unpack_grid(mx9_unpack_kernel<true>, nchunks, sms));
+  cfg.gridDim = dim3(dtype == MXQ_F32
+                         ? unpack_grid(mx9_unpack_kernel<false>, nb, UnpackShape<false>::kGroup, sms)
+                         : unpack_grid(mx9_unpack_kernel<true>, nb, UnpackShape<true>::kGroup, sms));
   cfg.blockDim = dim3(kUnpackBlock);
   cfg.stream = stream;
-  const uint32_t* q32 = reinterpret_cast<const uint32_t*>(q);
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
+  const uint4* q16 = reinterpret_cast<const uint4*>(q);
+  uint4* y16 = static_cast<uint4*>(y);
   const cudaError_t e =
       dtype == MXQ_F32
-          ? cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<false>, q32, max_exp, prime, y, nchunks)
-          : cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<true>, q32, max_exp, prime, y, nchunks);
+          ? cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<false>, q16, max_exp, prime, y16, nb)
+          : cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<true>, q16, max_exp, prime, y16, nb);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }

@@ -288,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t my = tiles_of_cta(static_cast<int64_t>(tiles_r) * tiles_c);
   if (tid == 0) init_barriers(bars, abort_flag);
   __syncthreads();
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -398,6 +400,8 @@ __global__ void __launch_bounds__(kUnpackThreads, 1)
   const int64_t my = tiles_of_cta(static_cast<int64_t>(tiles_r) * tiles_c);
   if (tid == 0) init_barriers(bars, abort_flag);
   __syncthreads();
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -558,6 +562,8 @@ int launch_wave(uint32_t smem, int64_t tiles, int threads, cudaStream_t stream, 
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 

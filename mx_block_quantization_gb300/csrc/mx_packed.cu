@@ -145,6 +145,8 @@ template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_pack_packed_kernel(const uint8_t* __restrict__ x, Geometry g, bool vec_rows,
                           bool packed_aligned, uint8_t* __restrict__ packed) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   using R = MxRule<Fmt<kFmt>::kOffset, Fmt<kFmt>::kQMax>;
   constexpr int RB = Fmt<kFmt>::kRecord;
   __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
@@ -207,6 +209,8 @@ template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_unpack_packed_kernel(const uint8_t* __restrict__ packed, Geometry g, bool vec_rows,
                             bool packed_aligned, uint8_t* __restrict__ y) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   constexpr int RB = Fmt<kFmt>::kRecord;
   __shared__ __align__(16) uint8_t stage[kWarps][32 * kMaxRecord];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -316,6 +320,8 @@ template <bool kBF16, int kFmt, bool kFlat>
 __global__ void __launch_bounds__(kThreads)
     mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
                              int64_t ld, uint8_t* __restrict__ y) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int kElems = kBF16 ? 8 : 4;  // elements per 16 output bytes
   constexpr int kParts = 16 / kElems;    // output units per block
@@ -474,6 +480,8 @@ template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_pack_cols_kernel(const uint8_t* __restrict__ x, Geometry g, bool packed_aligned,
                         uint8_t* __restrict__ packed) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   using T = ColTile<kBF16>;
   using R = MxRule<Fmt<kFmt>::kOffset, Fmt<kFmt>::kQMax>;
   constexpr int RB = Fmt<kFmt>::kRecord;
@@ -536,6 +544,8 @@ template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_unpack_cols_kernel(const uint8_t* __restrict__ packed, Geometry g, bool packed_aligned,
                           uint8_t* __restrict__ y) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   using T = ColTile<kBF16>;
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int kRun = 32 * kMaxRecord;  // staging bytes per column
@@ -727,6 +737,8 @@ template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_pack_cols_vec_kernel(const uint8_t* __restrict__ x, Geometry g, bool packed_aligned,
                             uint8_t* __restrict__ packed) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   using V = VecTile<kBF16>;
   using R = MxRule<Fmt<kFmt>::kOffset, Fmt<kFmt>::kQMax>;
   constexpr int RB = Fmt<kFmt>::kRecord;
@@ -846,6 +858,8 @@ template <bool kBF16, int kFmt>
 __global__ void __launch_bounds__(kThreads)
     mx_unpack_cols_vec_kernel(const uint8_t* __restrict__ packed, Geometry g, bool packed_aligned,
                               uint8_t* __restrict__ y) {
+  pdl_wait();  // inputs may be the previous kernel's output
+  pdl_trigger_at_start();
   using V = VecTile<kBF16>;
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int esize = kBF16 ? 2 : 4;
@@ -987,6 +1001,8 @@ int launch_cols(const Geometry& g, cudaStream_t stream, Args... args) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 
@@ -1032,6 +1048,8 @@ int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }
 

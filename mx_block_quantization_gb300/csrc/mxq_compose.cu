@@ -8,6 +8,7 @@
 // same GPU.  The composition writes the same bytes as the fused cast except in
 // colwise blocks that hold NaN: the separate 32x1 cast skips NaN in its amax
 // (description, NaN paragraph), the fused one poisons the block.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,6 +58,8 @@ __global__ void __launch_bounds__(kSwzThreads)
     mxq_swizzle_kernel(const uint8_t* __restrict__ s_rm, int64_t N, int64_t M,
                        const int32_t* __restrict__ offs, int G, uint8_t* __restrict__ s_col) {
   __shared__ int32_t s_offs[MXQ_MAX_GROUPS];
+  pdl_wait();  // s_rm is the previous kernel's output
+  pdl_trigger_at_start();
   int64_t end = M;
   if (offs != nullptr) {
     int bad = 0;
@@ -135,6 +138,8 @@ int launch_swizzle(const uint8_t* s_rm, int64_t N, int64_t M, const int32_t* off
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
   cfg.blockDim = dim3(kSwzThreads);
   cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, mxq_swizzle_kernel, s_rm, N, M, offs, static_cast<int>(G), s_col);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
@@ -213,17 +218,46 @@ namespace {
 // Every GPU that loads this library keeps it until the process exits.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MXQ_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the array on device `dev`, looked up once per device with
-// that device current (the host-side name is only a stand-in for the symbol).
+// The driver's cuCtxGetCurrent, reached through the runtime (no link-time
+// dependency on libcuda).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+// Device address of the array on device `dev` (the host-side name is only a
+// stand-in for the symbol).  It is looked up with that device current on the
+// first call, and again whenever the current context differs from the one it
+// was looked up in: after a device reset the module can load at another
+// address.  Later calls only compare the context, which is safe during a
+// stream capture; the lookup itself may load the module, so the first call on
+// a device (or in a new context) belongs before any capture.
 uint8_t* noalloc_scratch(int dev) {
   static std::mutex mu;
   static uint8_t* addr[64] = {};
+  static CUcontext ctx_of[64] = {};
   if (dev < 0 || dev >= 64) return nullptr;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return nullptr;
+  if (addr[dev] == nullptr || ctx == nullptr || ctx != ctx_of[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    // the lookup makes the device's primary context current if none was
+    if (get(&ctx) != CUDA_SUCCESS) return nullptr;
     addr[dev] = static_cast<uint8_t*>(p);
+    ctx_of[dev] = ctx;
   }
   return addr[dev];
 }

@@ -23,6 +23,44 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// A kernel launched with programmatic stream serialization may be scheduled
+// while the kernel before it on the stream is still running.  pdl_wait()
+// returns once that kernel has completed and its memory writes are visible
+// (at once when the launch has no such predecessor), so every kernel of the
+// library calls it, in every thread, before its first global-memory access.
+// Since no CTA gets past it early, a kernel never completes before its
+// predecessor, which keeps the ordering transitive along a chain of launches.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel of the stream (if launched with programmatic stream
+// serialization) be scheduled once every CTA of this grid has signalled or
+// exited; its CTAs then take SMs as this grid's CTAs leave and run their
+// set-up before their own pdl_wait().
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Where a kernel signals its dependents: 0 right after its set-up, 1 when a
+// thread has finished its main loop (threads without work exit instead), 2
+// never (the signal is then implied by the grid's completion).  2 is the
+// measured best: an explicit signal let the next kernel's CTAs become resident
+// beside the running ones, where they slowed it (the fp32 MX9 pack followed by
+// the unpack: 98 -> 105 us at 16384x8192 with the signal at set-up, 111 us
+// with it at the end of the main loops), while the kernels that follow gained
+// less than that.
+#ifndef MXQ_PDL_TRIGGER
+#define MXQ_PDL_TRIGGER 2
+#endif
+__device__ __forceinline__ void pdl_trigger_at_start() {
+  if (MXQ_PDL_TRIGGER == 0) pdl_launch_dependents();
+}
+__device__ __forceinline__ void pdl_trigger_at_end() {
+  if (MXQ_PDL_TRIGGER == 1) pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -309,7 +309,13 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
     sts32(base + kOffZero + 4u * tid, 0u);
     fence_proxy_async_smem();
   }
+  if (warp == R::kProducerWarp && lane == 0) tma_prefetch_desc(&tm_x);
   __syncthreads();
+  // The set-up above touched only shared memory and the launch parameters, so
+  // it may overlap the previous kernel of the stream; global memory may hold
+  // that kernel's results only from here on.
+  pdl_wait();
+  pdl_trigger_at_start();
 
   // Producer prologue: start the first loads before the offsets check.
   int64_t issued = 0;
@@ -336,7 +342,6 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
                       static_cast<uint32_t>((k / kStages) & 1));
   };
   if (is_producer) {
-    tma_prefetch_desc(&tm_x);
     for (; issued < my_tiles && issued < kStages; ++issued) issue_load(issued);
   }
 
@@ -388,6 +393,7 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.ofull(b));
     }
+    pdl_trigger_at_end();
   } else if (warp == R::kProducerWarp) {
     // -------------------------------------------------------------- producer
     if (lane == 0) {
@@ -401,6 +407,7 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
         issue_load(k);
         issued = k + 1;
       }
+      pdl_trigger_at_end();
     }
   } else if (warp == R::kStoreWarp) {
     // ---------------------------------------------------------------- storer
@@ -483,6 +490,7 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
         mbar_arrive(bars.oempty(b));
       }
     }
+    pdl_trigger_at_end();
     if (lane == 0) bulk_wait_all<0>();
   }
 }
@@ -569,6 +577,8 @@ int launch_tiles(const void* x, int64_t M, int64_t N, const int32_t* offs, int32
   cfg.blockDim = dim3(Roles<kMode>::kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, mxq_tile_kernel<kMode>, tm_x, tm_qrow, tm_qcol, offs,
                          static_cast<int>(G), static_cast<int>(M), static_cast<int>(N),
@@ -723,4 +733,8 @@ extern "C" int mxq_device_status(uint32_t* out, int clear) {
   if (rc != MXQ_OK) return rc;
   *out = v | w | c | t | k;
   return MXQ_OK;
+}
+
+extern "C" int mxq_last_device_status(uint32_t* out, int clear) {
+  return mxq_device_status(out, clear);
 }

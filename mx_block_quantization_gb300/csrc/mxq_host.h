@@ -39,6 +39,26 @@ inline bool ranges_overlap(const ByteRange* r, int n) {
   return false;
 }
 
+// Programmatic dependent launch of every compute kernel (on by default; the
+// macro exists so that a build without it can be measured against).
+#ifndef MXQ_PDL
+#define MXQ_PDL 1
+#endif
+
+// Marks a launch as allowed to start while the previous kernel of its stream
+// is still running.  The kernel must call pdl_wait() (mxq_device.cuh) before
+// touching global memory; with the attribute set, a predecessor that calls
+// pdl_launch_dependents() lets this launch's CTAs be placed on SMs as its
+// own CTAs leave, which hides the launch latency and set-up between kernels.
+// `attr` must outlive the cudaLaunchKernelEx call.
+inline void allow_programmatic_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr) {
+  if (!MXQ_PDL) return;
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
 // Number of SMs of the current device, cached per device ordinal.
 inline int sm_count_current_device(int* out_device) {
   static std::atomic<int> cache[64];
