@@ -114,8 +114,8 @@ uint8_t oracle_e4m3_encode(double v) {
 }
 
 /* ------------------------------------------------------------------------- */
-/* E8M0 "rceil" scale ([AO] description: "rceil only"; review reply on the    */
-/* scale 0/1 cutoff 448*2^-127).                                              */
+/* E8M0 rceil scale (the [AO] description supports the rceil rounding mode   */
+/* alone; review reply on the scale 0/1 cutoff 448*2^-127).                   */
 /* ------------------------------------------------------------------------- */
 
 /*
@@ -237,9 +237,9 @@ int64_t oracle_blocked_index(int64_t r, int64_t c, int64_t R, int64_t C) {
 /* ------------------------------------------------------------------------- */
 
 /*
- * Validation of the group offsets ([AO] description: "every group size must
- * be a multiple of 128"; review replies: offsets are checked for ordering and
- * bounds; empty groups are valid).  offs == NULL selects dense placement and
+ * Validation of the group offsets (the [AO] description requires each group
+ * size to be a multiple of 128; review replies: offsets are checked for
+ * ordering and bounds; empty groups are valid).  offs == NULL selects dense placement and
  * then G must be 0.
  */
 int oracle_check_offs(const int32_t *offs, int32_t G, int64_t M) {
@@ -260,13 +260,13 @@ int oracle_check_offs(const int32_t *offs, int32_t G, int64_t M) {
  *   q_row [M*N]      E4M3, q_row[m*N + n]            (1x32 blocks along N)
  *   s_row [M*N/32]   E8M0, blocked as an [M, N/32] scale matrix
  *   q_col [N*M]      E4M3, q_col[n*M + m]            (32x1 blocks along M,
- *                    stored logically transposed -- [AO] description:
- *                    "logically transposed colwise store")
+ *                    stored transposed, as the [AO] description's
+ *                    colwise store is)
  *   s_col [N*M/32]   E8M0 colwise scales grouped by offs:
  *       group g covers rows [lo, hi) = [offs[g-1] (0 for g = 0), offs[g]);
  *       its scales form an [N, (hi-lo)/32] matrix, blocked, stored as one
- *       contiguous slab starting at byte N*lo/32 (READING of the "slab" and
- *       "compact column scales" wording);
+ *       contiguous slab starting at byte N*lo/32 (READING of the [AO]
+ *       description's per-group slabs and compact column scales);
  *       every byte from N*offs[G-1]/32 to the end is 0 ([AO] description,
  *       "Uncovered tail": rows past offs[-1] are still quantized, their column
  *       scale bytes are zeroed).
@@ -378,8 +378,9 @@ int oracle_swizzle_kgroups(const uint8_t *s_rm, int64_t N, int64_t M, const int3
 /* ------------------------------------------------------------------------- */
 
 /*
- * Element exponent taken from the native bits ([MX9] "Exponent extracted from
- * native dtype bits"): the biased exponent field minus 127, so zero and
+ * Element exponent taken from the native bits ([MX9] "Key design choices":
+ * the exponent comes from the input type's own bit fields): the biased
+ * exponent field minus 127, so zero and
  * subnormals give -127 and Inf/NaN give 128.
  */
 static int mx9_t(const void *x, int dtype, int64_t idx) {
@@ -401,8 +402,8 @@ static double mx9_value(const void *x, int dtype, int64_t idx) {
  * Scale exponent of pair p: the shared exponent E less 6 (8-bit signed
  * elements with 7 magnitude bits cover |x| < 2^(E+1)), less one more for a
  * pair flagged in the prime bitmap, clamped below at -126, the smallest fp32
- * normal exponent ([MX9] "Scale exponent clamped to -126").
- * READING: the offset 6 and the prime polarity are fixed by "9 bits/element"
+ * normal exponent ([MX9] "Key design choices").
+ * READING: the offset 6 and the prime polarity are fixed by nine bits per element
  * (8-bit value, 1/2 bit shared exponent, 1/2 bit prime) and by the quality the
  * page reports; the page does not print them.
  */
@@ -419,7 +420,7 @@ static int mx9_k(int E, int tau) {
  *   q[16b + i] = clamp(round_half_even(x_i / 2^k_p), -127, 127)
  * The division is by a power of two, hence exact ([MX9] review: IEEE
  * round-nearest division), and the rounding is ties-to-even.  The clamp is
- * symmetric ([MX9] "Symmetric clamp +-127").
+ * symmetric at +-127 ([MX9] "Key design choices").
  * READING for non-finite inputs (the page only says NaN produces garbage):
  * NaN packs to q = 0; +-Inf to +-127; the block's max_exp is 255.
  */
@@ -505,11 +506,10 @@ int oracle_mx9_unpack(const int8_t *q, const uint8_t *max_exp,
 
 /* ------------------------------------------------------------------------- */
 /* MX9 and MX6 in the single packed tensor, blocked along either axis of a    */
-/* strided 2-D tensor, with a zero-padded partial last block ([MX9] review:   */
-/* "pack mx9 into a single uint8 tensor and dispatch mx6/mx9 to the packed     */
-/* kernels", "consume strided quantization inputs", the axis and padding      */
-/* tests of the suite; the exponent byte is stored at the block record's      */
-/* start).                                                                     */
+/* strided 2-D tensor, with a zero-padded partial last block ([MX9] commits: */
+/* MX9 packed into one uint8 tensor with MX6 and MX9 sent to the packed       */
+/* kernels, strided inputs accepted; the axis and padding tests of the suite; */
+/* the exponent byte is stored at the block record's start).                  */
 /*                                                                             */
 /* READINGS: a record is [exponent byte, prime byte, data]; MX9 data is the    */
 /* 16 int8 q; MX6 uses the same rule with 4 magnitude bits (offset 3 instead   */
