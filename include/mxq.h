@@ -262,6 +262,30 @@ int mxq_quantize_2d_dual_3pass_noalloc(const void *x, int64_t M, int64_t N, cons
                                        uint8_t *s_col, cudaStream_t stream);
 
 /*
+ * Block-scaled MXFP8 matrix product on the tensor cores, reading E4M3 rows and
+ * E8M0 scale matrices exactly as mxq_quantize_2d_dual stores them: the consumer
+ * check of the layouts ([AO] description, first paragraph: the scales are
+ * written in the blocked form the block-scaled MMA reads; "Uncovered tail"
+ * paragraph: one slab per K-group).  tcgen05.mma of kind mxf8f6f4 with one
+ * E8M0 scale per 32 K elements; a checking tool, not a tuned GEMM (one CTA per
+ * 128x128 output tile, no overlap of loads and MMAs).
+ *   D[i, j] = sum_k A(i, k) * 2^(sa(i, k/32) - 127) * B(j, k) * 2^(sb(j, k/32) - 127)
+ *   a      E4M3 [Ma, K], row i at a + i*lda (K contiguous bytes); e.g. q_row
+ *          (lda = N), or a K-group's columns of q_col (a = q_col + lo, lda = M).
+ *   sa     E8M0 [Ma, K/32] in the 128x4 blocked layout (s_row, or the group's
+ *          s_col slab at s_col + N*lo/32).
+ *   b, ldb, sb   likewise for B [Nb, K].
+ *   d      fp32 [Ma, Nb] row-major.
+ *   Ma, Nb, K    multiples of 128, at most 2^24 (Ma == 0 or Nb == 0: no-op;
+ *          K == 0 with Ma, Nb > 0: MXQ_EBADSHAPE); lda, ldb >= K and multiples of
+ *          16; every pointer 16-byte aligned; d must not overlap an input.
+ * Every internal wait is bounded (MXQ_DEV_TIMEOUT in the status word).
+ */
+int mxq_mxfp8_scaled_mm(const uint8_t *a, int64_t lda, const uint8_t *sa, const uint8_t *b,
+                        int64_t ldb, const uint8_t *sb, float *d, int64_t Ma, int64_t Nb, int64_t K,
+                        cudaStream_t stream);
+
+/*
  * Device status word of the current device: a sticky OR of MXQ_DEV_* bits set
  * by kernels since the last clear.  Writes it to *out and clears it when
  * `clear` is non-zero.  This call synchronizes the device (it reads device

@@ -21,6 +21,9 @@ Operations (sources by page title):
 * :func:`quantize_1x32`, :func:`quantize_32x1`, :func:`swizzle_kgroups`,
   :func:`quantize_2d_dual_3pass` -- the three-pass composition the fused cast
   replaces (pytorch/ao PR #4995, first paragraph), for comparison.
+* :func:`mxfp8_scaled_mm` -- a block-scaled MXFP8 product on the tensor cores
+  (tcgen05) that reads the cast's bytes as stored: the consumer check of the
+  blocked scale layouts and the K-group slabs.
 
 With MXQ_CHECKED=1 in the environment the binding loads libmxq_checked.so,
 the same kernels with every computed global access tested against its buffer.
@@ -103,6 +106,10 @@ def lib() -> ctypes.CDLL:
         L.mx_unpack_packed.restype = ctypes.c_int
         L.mx_unpack_packed.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i64, i64, i64,
                                        ctypes.c_int, vp]
+        L.mxq_mxfp8_scaled_mm.restype = ctypes.c_int
+        L.mxq_mxfp8_scaled_mm.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i64, i64, vp]
+        L.mxq_last_device_status.restype = ctypes.c_int
+        L.mxq_last_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.mxq_selftest_wait_timeout.restype = ctypes.c_int
         L.mxq_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         L.mxq_debug_bounds.restype = ctypes.c_int
@@ -514,3 +521,42 @@ def mx_unpack_packed(packed, fmt: int, out, axis: int = 1, *, stream=None):
     if rc != OK:
         raise MxqError(rc, "mx_unpack_packed")
     return out
+
+
+# ---------------------------------------------------------------------------
+# consumer check of the layouts: a block-scaled MXFP8 product on the tensor cores
+# ---------------------------------------------------------------------------
+
+def mxfp8_scaled_mm(a, sa, b, sb, *, out=None, stream=None):
+    """fp32 [Ma, Nb] = (a scaled by sa) @ (b scaled by sb)^T on tcgen05.
+
+    ``a``: uint8 E4M3 [Ma, K] CUDA tensor whose rows may be strided (unit column
+    stride, row stride a multiple of 16), e.g. ``q_row`` or the K-group columns
+    ``q_col[:, lo:hi]``; ``sa``: uint8 E8M0 [Ma*K/32] in the 128x4 blocked layout
+    (``s_row``, or the group's slab of ``s_col``).  Likewise ``b``/``sb``.
+    Ma, Nb, K multiples of 128."""
+    torch = _torch()
+    ma, k, lda = _view_2d(a, "a")
+    nb, kb, ldb = _view_2d(b, "b")
+    if k != kb:
+        raise ValueError(f"a and b disagree on K: {k} vs {kb}")
+    for t, name, n in ((sa, "sa", ma * k // 32), (sb, "sb", nb * k // 32)):
+        _check_cuda(t, name)
+        if t.dtype != torch.uint8 or t.numel() != n:
+            raise ValueError(f"{name} must be uint8 with {n} bytes")
+    if a.dtype != torch.uint8 or b.dtype != torch.uint8:
+        raise ValueError("a and b must be uint8 E4M3 bytes")
+    if out is None:
+        out = torch.empty((ma, nb), dtype=torch.float32, device=a.device)
+    _check_cuda(out, "out")
+    if out.dtype != torch.float32 or tuple(out.shape) != (ma, nb):
+        raise ValueError(f"out must be float32 [{ma}, {nb}]")
+    vp = ctypes.c_void_p
+    with torch.cuda.device(a.device):
+        rc = lib().mxq_mxfp8_scaled_mm(vp(a.data_ptr()), lda, vp(sa.data_ptr()), vp(b.data_ptr()), ldb,
+                                       vp(sb.data_ptr()), vp(out.data_ptr()), ma, nb, k,
+                                       _stream_handle(a.device, stream))
+    if rc != OK:
+        raise MxqError(rc, "mxq_mxfp8_scaled_mm")
+    return out
+

@@ -27,7 +27,8 @@ STAMP = BUILD_DIR / "libmxq.stamp"
 CHECKED_LIB_PATH = PKG / "libmxq_checked.so"
 CHECKED_FLAGS = ["-DMXQ_DEBUG_BOUNDS=1"]
 
-SOURCES = ["mxq_dual.cu", "mxq_compose.cu", "mx9.cu", "mx_packed.cu", "mx_cols_tma.cu", "mxq_abi.cpp"]
+SOURCES = ["mxq_dual.cu", "mxq_compose.cu", "mx9.cu", "mx_packed.cu", "mx_cols_tma.cu", "mxq_mma_check.cu",
+           "mxq_abi.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-diag-suppress", "177", f"-I{INCLUDE}", f"-I{CSRC}"]

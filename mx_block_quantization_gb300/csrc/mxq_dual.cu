@@ -710,6 +710,7 @@ int mx9_status_read(unsigned int* out, bool clear);      // mx9.cu
 int compose_status_read(unsigned int* out, bool clear);  // mxq_compose.cu
 int cols_status_read(unsigned int* out, bool clear);     // mx_cols_tma.cu
 int packed_status_read(unsigned int* out, bool clear);   // mx_packed.cu
+int mma_status_read(unsigned int* out, bool clear);      // mxq_mma_check.cu
 }
 
 // The device status word is the OR of the per-file words of the kernels.
@@ -731,7 +732,10 @@ extern "C" int mxq_device_status(uint32_t* out, int clear) {
   if (rc != MXQ_OK) return rc;
   rc = mxq::packed_status_read(&k, clear != 0);
   if (rc != MXQ_OK) return rc;
-  *out = v | w | c | t | k;
+  unsigned int g = 0;
+  rc = mxq::mma_status_read(&g, clear != 0);
+  if (rc != MXQ_OK) return rc;
+  *out = v | w | c | t | k | g;
   return MXQ_OK;
 }
 
