@@ -100,7 +100,9 @@ def profiled_traffic():
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+    BUSY_PCT = 50.0  # samples below this utilization are idle moments, left out of the median
 
     def __init__(self, device_index: int):
         self.dev = device_index
@@ -124,7 +126,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, reasons, total = [], [], set(), 0
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         try:
             rows = open(self.path).read().strip().splitlines()
@@ -135,20 +137,29 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                clk, clk_max = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
+            total += 1
+            # a throttle reason counts whenever it shows; the clock median only
+            # over samples taken while the GPU was busy (utilization, when given)
             for name, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(name)
+            try:
+                busy = float(parts[9]) >= self.BUSY_PCT if len(parts) > 9 else True
+            except ValueError:
+                busy = True
+            if busy:
+                sm.append(clk)
+                smax.append(clk_max)
         try:
             os.remove(self.path)
         except OSError:
             pass
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "samples_all": total, "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -524,7 +535,6 @@ def run_gpu(args):
                            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
                            "algorithmic_bytes": sb[name],
                            "isolated": {"us": iso, "gbs": iso_gbs, "frac_of_measured": iso_gbs / peak}}
-    clocks = sampler.stop()
     assert mxq.device_status(clear=True) == 0
     achieved = breakdown["mxq_dual"]["gbs"]
     roofline = {"bound": "hbm", "kernel": "mxq_tile_kernel<kDual>", "achieved": achieved, "peak": peak,
@@ -542,6 +552,10 @@ def run_gpu(args):
     configs = None
     if rank == 0 and not args.no_configs:
         configs = measure_configs(mxq, torch, dev, peak)
+    # the clock record spans the warm-up, the timed region, the per-kernel
+    # passes and the configs (the timed region alone is a few ms at small K)
+    clocks = sampler.stop()
+    clocks["window"] = "warm-up through the per-workload figures; busy samples only"
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, mxq, torch, dev, cur, xd_h, offs, xm_h, dual_out, (q, e, p), y, world)
@@ -832,6 +846,14 @@ def run_case(args):
                 mxq.quantize_2d_dual(x, offs, out=out)
             else:
                 mxq.quantize_2d_dual_3pass(x, offs, workspace=ws, out=out)
+    elif args.case == "mma":
+        # the tensor-core consumer check on the cast of an [M, N] tensor: q_row
+        # and s_row against themselves (K = N)
+        x = torch.from_numpy(W.normal_bf16((M, N), seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+        out = mxq.quantize_2d_dual(x)
+        d = torch.empty((M, M), dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            mxq.mxfp8_scaled_mm(out.q_row, out.s_row, out.q_row, out.s_row, out=d)
     elif args.case.startswith("rec_"):
         # the single packed tensor of MX9 (--fmt 9) or MX6 (--fmt 6) records, rows blocked
         tdt = torch.float32 if args.case.endswith("f32") else torch.bfloat16
@@ -873,7 +895,7 @@ def main(argv=None):
                     help="skip the per-workload graph-replay figures of the JSON line's configs key")
     ap.add_argument("--sweep", action="store_true",
                     help="also print one line per packed-tensor geometry (graph replay)")
-    ap.add_argument("--case", choices=["dual", "dual3", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16",
+    ap.add_argument("--case", choices=["dual", "dual3", "mma", "pack_f32", "pack_bf16", "unpack_f32", "unpack_bf16",
                                        "rec_pack_f32", "rec_pack_bf16", "rec_unpack_f32",
                                        "rec_unpack_bf16"],
                     help="only launch this kernel --warmup times on --shape (profiling)")

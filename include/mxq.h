@@ -277,8 +277,9 @@ int mxq_quantize_2d_dual_3pass_noalloc(const void *x, int64_t M, int64_t N, cons
  *   b, ldb, sb   likewise for B [Nb, K].
  *   d      fp32 [Ma, Nb] row-major.
  *   Ma, Nb, K    multiples of 128, at most 2^24 (Ma == 0 or Nb == 0: no-op;
- *          K == 0 with Ma, Nb > 0: MXQ_EBADSHAPE); lda, ldb >= K and multiples of
- *          16; every pointer 16-byte aligned; d must not overlap an input.
+ *          K == 0 with Ma, Nb > 0: MXQ_EBADSHAPE); lda, ldb >= K, multiples of 16
+ *          and at most 2^40; every pointer 16-byte aligned; d must not overlap an
+ *          input.
  * Every internal wait is bounded (MXQ_DEV_TIMEOUT in the status word).
  */
 int mxq_mxfp8_scaled_mm(const uint8_t *a, int64_t lda, const uint8_t *sa, const uint8_t *b,

@@ -241,7 +241,10 @@ extern "C" int mxq_mxfp8_scaled_mm(const uint8_t* a, int64_t lda, const uint8_t*
       Ma > (int64_t{1} << 24) || Nb > (int64_t{1} << 24) || K > (int64_t{1} << 24))
     return MXQ_EBADSHAPE;
   if (Ma == 0 || Nb == 0) return MXQ_OK;
-  if (K == 0 || lda < K || ldb < K || lda % 16 != 0 || ldb % 16 != 0) return MXQ_EBADSHAPE;
+  // row pitches bounded so that no byte range below can wrap
+  if (K == 0 || lda < K || ldb < K || lda % 16 != 0 || ldb % 16 != 0 ||
+      lda > (int64_t{1} << 40) || ldb > (int64_t{1} << 40))
+    return MXQ_EBADSHAPE;
   if (!a || !sa || !b || !sb || !d) return MXQ_ENULL;
   if (!aligned_to(a, 16) || !aligned_to(sa, 16) || !aligned_to(b, 16) || !aligned_to(sb, 16) ||
       !aligned_to(d, 16))

@@ -103,6 +103,22 @@ for _ in range(N_CASES):
     expect("mx_pack_packed", rc, want, (rows, cols, ld, axis, fmt, dt))
     rc = L.mx_unpack_packed(vp(BASE[1]), fmt, vp(BASE[0]), dt, rows, cols, ld, axis, None)
     expect("mx_unpack_packed", rc, want, (rows, cols, ld, axis, fmt, dt))
+    # the tensor-core consumer check: Ma, Nb, K multiples of 128 up to 2^24, row pitches
+    Ma, Nb, K = pick(), pick(), pick()
+    lda = K + int(g.integers(0, 3)) * 16 if g.random() < 0.7 else pick()
+    ldb = K if g.random() < 0.7 else pick()
+    dims_ok = all(v >= 0 and v % 128 == 0 and v <= (1 << 24) for v in (Ma, Nb, K))
+    rc = L.mxq_mxfp8_scaled_mm(vp(BASE[0]), lda, vp(BASE[1]), vp(BASE[2]), ldb, vp(BASE[3]),
+                               vp(BASE[4]), Ma, Nb, K, None)
+    if not dims_ok:
+        want = {mxq.EBADSHAPE}
+    elif Ma * Nb == 0:
+        want = {mxq.OK}
+    elif K == 0 or not all(l >= K and l % 16 == 0 and l <= (1 << 40) for l in (lda, ldb)):
+        want = {mxq.EBADSHAPE}
+    else:
+        want = {mxq.ECUDA, mxq.EOVERLAP}
+    expect("mxfp8_scaled_mm", rc, want, (Ma, Nb, K, lda, ldb))
 # bands placed past int64 range by their start (row0 + rows would wrap)
 for row0 in (I64_MAX - 127, I64_MAX - 255, (1 << 62) + 128, (1 << 31) * 128):
     for rows in (128, 256, 1 << 30):
