@@ -49,7 +49,7 @@ using namespace mxq;
 #define MXQ_DUAL_GROUP_ROWS 8
 #endif
 // When the fused cast issues each tile's s_col atom store: 1 once the tile's
-// data stores (q_row, s_row, q_col) have read their shared-memory tiles, from a
+// data stores (q_row, q_col) have read their shared-memory tiles, from a
 // 4-slot ring of atoms so that the data buffer is still released at that point;
 // 0 together with the data stores.  1 measured 3.5-6% faster on grouped
 // layouts at 65536x7168 (MoE groups 0.943 -> 0.976 of the measured copy rate,
@@ -58,6 +58,13 @@ using namespace mxq;
 #ifndef MXQ_DUAL_SCOL_DEFER
 #define MXQ_DUAL_SCOL_DEFER 1
 #endif
+// 1: the s_row atom goes after the data stores too, from its own 4-slot ring
+// (grouped layouts at 65536x7168: MoE 0.974 -> 0.982 of the measured copy rate,
+// 64 groups 0.965 -> 0.983; dense unchanged)
+#ifndef MXQ_DUAL_SROW_AFTER
+#define MXQ_DUAL_SROW_AFTER 1
+#endif
+constexpr bool kSRowAfter = MXQ_DUAL_SCOL_DEFER && MXQ_DUAL_SROW_AFTER;
 #ifndef MXQ_DUAL_L2_HINTS  // bit 0: evict-first on the input loads, bit 1: on the data stores
 #define MXQ_DUAL_L2_HINTS 0
 #endif
@@ -96,7 +103,8 @@ constexpr uint32_t kOffSRow = kOffQCol + kOutBufs * kQTileBytes;
 constexpr uint32_t kOffSCol = kOffSRow + kOutBufs * kAtomBytes;
 constexpr int kSColSlots = 4;                          // deferred s_col atoms
 constexpr uint32_t kOffSColRing = kOffSCol + kOutBufs * kAtomBytes;
-constexpr uint32_t kOffZero = kOffSColRing + kSColSlots * kAtomBytes;
+constexpr uint32_t kOffSRowRing = kOffSColRing + kSColSlots * kAtomBytes;
+constexpr uint32_t kOffZero = kOffSRowRing + (kSRowAfter ? kSColSlots : 0) * kAtomBytes;
 constexpr uint32_t kOffOffs = kOffZero + kAtomBytes;
 constexpr uint32_t kOffBar = kOffOffs + 4 * MXQ_MAX_GROUPS;
 constexpr uint32_t kNumBars = 2 * kStages + 2 * kOutBufs;
@@ -394,7 +402,10 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
       if (!__all_sync(0xFFFFFFFFu, ok)) return;
       const uint32_t in_s = base + kOffIn + static_cast<uint32_t>(s) * kInStageBytes;
       if (warp < R::kRowWarps)
-        rowwise_pass(in_s, base + kOffQRow + b * kQTileBytes, base + kOffSRow + b * kAtomBytes,
+        rowwise_pass(in_s, base + kOffQRow + b * kQTileBytes,
+                     (kMode == kDual && kSRowAfter)
+                         ? base + kOffSRowRing + static_cast<uint32_t>(k % kSColSlots) * kAtomBytes
+                         : base + kOffSRow + b * kAtomBytes,
                      warp, lane);
       else
         colwise_pass<kMode == kDual>(
@@ -467,7 +478,8 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
           else
             tma_store_2d(&tm_qrow, static_cast<int32_t>(tj * kTile), static_cast<int32_t>(row0),
                          base + kOffQRow + b * kQTileBytes);
-          if (in_buf(s_row + (ti * TN + tj) * kAtomBytes, kAtomBytes, s_row,
+          if (!(kMode == kDual && kSRowAfter) &&
+              in_buf(s_row + (ti * TN + tj) * kAtomBytes, kAtomBytes, s_row,
                      static_cast<uint64_t>(N) * Mrows / 32, &g_mxq_status))
             bulk_store(s_row + (ti * TN + tj) * kAtomBytes, base + kOffSRow + b * kAtomBytes,
                        kAtomBytes);
@@ -513,6 +525,11 @@ __global__ void __launch_bounds__(Roles<kMode>::kThreads, 1)
             bulk_commit();
             bulk_wait_read<0>();
             if (dst != nullptr) bulk_store(dst, src, kAtomBytes);
+            if (kSRowAfter && in_buf(s_row + (ti * TN + tj) * kAtomBytes, kAtomBytes, s_row,
+                                     static_cast<uint64_t>(N) * Mrows / 32, &g_mxq_status))
+              bulk_store(s_row + (ti * TN + tj) * kAtomBytes,
+                         base + kOffSRowRing + static_cast<uint32_t>(k % kSColSlots) * kAtomBytes,
+                         kAtomBytes);
             bulk_commit();
           } else {
             if (dst != nullptr) bulk_store(dst, src, kAtomBytes);
