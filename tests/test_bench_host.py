@@ -64,3 +64,18 @@ def test_traffic_is_reported_only_for_the_profiled_source(tmp_path, monkeypatch)
     assert bench.profiled_traffic() is None
     monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(tmp_path / "missing.md"))
     assert bench.profiled_traffic() is None
+
+
+def test_clock_sampler_leaves_idle_samples_out_of_the_median(tmp_path, monkeypatch):
+    rows = ["0, 1980, 2070, 190.0, 0x0, Not Active, Not Active, Not Active, Not Active, 0",
+            "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active, 97",
+            "0, 2055, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Active, 100",
+            "0, 1500, 2070, 200.0, 0x0, Not Active, Not Active, Not Active, Not Active, 3"]
+    monkeypatch.setenv("PATH", _fake_smi(tmp_path, rows) + os.pathsep + os.environ["PATH"])
+    s = bench.ClockSampler(0)
+    s.start()
+    time.sleep(0.5)
+    r = s.stop()
+    assert r["samples"] == 2 and r["samples_all"] == 4
+    assert r["sm_mhz"] == (2070.0 + 2055.0) / 2
+    assert r["reasons"] == ["sw_power_cap"]
