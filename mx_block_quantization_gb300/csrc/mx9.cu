@@ -22,8 +22,11 @@
 // staging each warp's 32 records and storing them with one bulk copy.
 // unpack: a streaming kernel, one wave of resident blocks; each lane decodes
 // whole 16-element blocks (exact q * 2^k built without conversion
-// instructions) and a per-warp shared-memory transpose turns them into
-// 512-byte contiguous stores.
+// instructions) into a per-warp shared-memory stage, from which a warp's
+// round of 32 blocks leaves as one tensor store (fp32 output) or as 512-byte
+// contiguous lane stores (bf16 output).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -99,6 +102,34 @@ using namespace mxq;
 // back but 1-2% slower in the step, after the pack or the dual cast.
 #ifndef MXQ_MX9_UNPACK_KIND
 #define MXQ_MX9_UNPACK_KIND 2
+#endif
+
+// Unpack stores, per output type: 1 = each warp's decoded round leaves
+// shared memory as one tensor store (TMA) of whole 128-byte rows, 0 = lane
+// stores of 16 bytes.  Measured on GB300 at 16384x8192 and 32768x16384: the
+// tensor store is 2-5% faster for fp32 (2 KB per round) and 7-9% slower for
+// bf16 (1 KB per round, at 64 or 80 registers alike); 3 slots for fp32, or
+// unrolling 1 or 4 rounds, or 5 blocks per SM were all slower.
+#ifndef MXQ_MX9_UNPACK_TMA_F32
+#define MXQ_MX9_UNPACK_TMA_F32 1
+#endif
+#ifndef MXQ_MX9_UNPACK_TMA_BF16
+#define MXQ_MX9_UNPACK_TMA_BF16 0
+#endif
+// Minimum resident blocks per SM asked of the register allocator (0: none).
+#ifndef MXQ_MX9_UNPACK_MINB_F32
+#define MXQ_MX9_UNPACK_MINB_F32 0
+#endif
+#ifndef MXQ_MX9_UNPACK_MINB_BF16
+#define MXQ_MX9_UNPACK_MINB_BF16 0
+#endif
+// Staging slots per warp for the tensor-store form (a slot is rewritten once
+// the store issued from it kSlots rounds earlier has read it).
+#ifndef MXQ_MX9_UNPACK_SLOTS_F32
+#define MXQ_MX9_UNPACK_SLOTS_F32 2
+#endif
+#ifndef MXQ_MX9_UNPACK_SLOTS_BF16
+#define MXQ_MX9_UNPACK_SLOTS_BF16 4
 #endif
 
 constexpr int kUnpackBlock = 256;
@@ -352,26 +383,35 @@ __device__ __forceinline__ float small_int_to_float(int32_t q) {
 // round are 512 contiguous q bytes and 32 contiguous bytes of each of the
 // others), kUnroll rounds' loads issued before the first decode.  The decoded
 // block (64 bytes of fp32 or 32 of bf16) goes to a per-warp staging buffer in
-// shared memory, from which each lane stores 16-byte pieces so that every
-// store instruction writes 512 contiguous output bytes.  q * 2^k is exact
-// (|q| <= 127, k >= -126) except for overflow in max_exp 255 blocks; a bf16
-// result has at most 7 significant bits, so the top half of the fp32 is the
-// exact bf16.
-template <bool kBF16>
+// shared memory, from which the round's 32 blocks (2 KB fp32, 1 KB bf16, one
+// contiguous stretch of the output) leave either as one tensor store (TMA)
+// or as lane stores of 16-byte pieces, every instruction writing 512
+// contiguous bytes.  q * 2^k is exact (|q| <= 127, k >= -126) except for
+// overflow in max_exp 255 blocks; a bf16 result has at most 7 significant
+// bits, so the top half of the fp32 is the exact bf16.
+template <bool kBF16, bool kTma>
 struct UnpackShape {
   static constexpr int kChunks = kBF16 ? 2 : 4;  // 16-byte output pieces per block
   static constexpr int kUnroll = kBF16 ? MXQ_MX9_UNPACK_UNROLL_BF16 : MXQ_MX9_UNPACK_UNROLL_F32;
   static constexpr int kWarps = kUnpackBlock / 32;
   static constexpr int kGroup = 32 * kUnroll;                   // blocks per warp iteration
   static constexpr uint32_t kStageBytes = 32u * kChunks * 16u;  // one round of a warp
+  static constexpr int kRows = 32 * kChunks / 8;                // 128-byte output rows per round
+  static constexpr int kSlots =
+      kTma ? (kBF16 ? MXQ_MX9_UNPACK_SLOTS_BF16 : MXQ_MX9_UNPACK_SLOTS_F32) : 1;
+  static_assert(kStageBytes % 1024 == 0, "a slot keeps the 1024-byte swizzle period");
 };
 
 // Slot of output piece c (piece c % kChunks of the round's block c / kChunks)
-// in a warp's staging buffer.  XOR-ing bits 3.. of c into its low bits makes
-// both access patterns conflict-free: the writes, where lane l stores the
-// pieces of its own block, and the reads, where lane l loads piece 32r + l.
-template <bool kBF16>
+// in a warp's staging buffer.  Lane stores: XOR-ing bits 3.. of c into its
+// low bits makes both access patterns conflict-free: the writes, where lane l
+// stores the pieces of its own block, and the reads, where lane l loads piece
+// 32r + l.  Tensor store: the 128-byte swizzle of the tensor map (16-byte
+// column c % 8 of 128-byte row c / 8 sits at column (c % 8) ^ (row % 8)),
+// under which the writes are conflict-free as well.
+template <bool kBF16, bool kTma>
 __device__ __forceinline__ uint32_t unpack_slot(int c) {
+  if (kTma) return static_cast<uint32_t>((c & ~7) | ((c ^ (c >> 3)) & 7));
   return static_cast<uint32_t>(kBF16 ? c ^ ((c >> 3) & 1) : c ^ ((c >> 3) & 3));
 }
 
@@ -396,18 +436,28 @@ __device__ __forceinline__ void unpack4_biased(uint32_t vx, float s0, float s1, 
   y[3] = fmul_rn_noftz(fadd_rn_noftz(__uint_as_float(__byte_perm(vx, 0x4B000000u, 0x7653)), -kBias), s1);
 }
 
-template <bool kBF16>
-__global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
-    const uint4* __restrict__ q, const uint8_t* __restrict__ max_exp,
-    const uint8_t* __restrict__ prime, uint4* __restrict__ y, int64_t nb) {
-  using U = UnpackShape<kBF16>;
-  __shared__ __align__(16) uint8_t stage[U::kWarps][U::kStageBytes];
+// tm_y (tensor-store form only) views the output as `rows_y` rows of 128
+// bytes (32 uint32 words), box kRows rows, 128-byte swizzle; the bytes past
+// the last whole row (under 128) are written by lane stores.
+template <bool kBF16, bool kTma>
+__global__ void __launch_bounds__(kUnpackBlock,
+                                  kBF16 ? MXQ_MX9_UNPACK_MINB_BF16 : MXQ_MX9_UNPACK_MINB_F32)
+    mx9_unpack_kernel(
+    const __grid_constant__ CUtensorMap tm_y, const uint4* __restrict__ q,
+    const uint8_t* __restrict__ max_exp, const uint8_t* __restrict__ prime,
+    uint4* __restrict__ y, int64_t nb, int64_t rows_y) {
+  using U = UnpackShape<kBF16, kTma>;
+  __shared__ __align__(1024) uint8_t stage[U::kWarps][U::kSlots][U::kStageBytes];
+  if (kTma && threadIdx.x == 0) tma_prefetch_desc(&tm_y);
   pdl_wait();
   pdl_trigger_at_start();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t st = smem_u32(stage[warp]);
   const int64_t gwarps = static_cast<int64_t>(gridDim.x) * U::kWarps;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * U::kWarps + warp;
+  const int64_t npieces = nb * U::kChunks;
+  // the swizzle assumes 1024-byte aligned slots; were the array placed
+  // otherwise, every piece would leave by lane stores instead
+  if (kTma && (smem_u32(stage) & 1023u) != 0) rows_y = 0;
   // first block of round u of iteration it: a warp's own group of kUnroll
   // rounds, or grid-wide rounds (all warps' round u adjacent)
   auto round_base = [&](int64_t it, int u) -> int64_t {
@@ -434,6 +484,13 @@ __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
     for (int u = 0; u < U::kUnroll; ++u) {
       const int64_t bu = round_base(it, u);  // first block of the round (warp-uniform)
       if (bu >= nb) break;
+      const uint32_t st =
+          smem_u32(stage[warp][kTma ? static_cast<int>((it * U::kUnroll + u) % U::kSlots) : 0]);
+      if (kTma) {
+        // the store issued from this slot kSlots rounds ago has read it
+        if (lane == 0) bulk_wait_read<U::kSlots - 1>();
+        __syncwarp();
+      }
       const int E = static_cast<int>(ev[u]) - 127;
       const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
       float v[16];  // word k holds elements 4k..4k+3, i.e. pairs 2k and 2k+1
@@ -453,7 +510,7 @@ __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
       }
 #pragma unroll
       for (int j = 0; j < U::kChunks; ++j) {
-        const uint32_t a = st + 16u * unpack_slot<kBF16>(U::kChunks * lane + j);
+        const uint32_t a = st + 16u * unpack_slot<kBF16, kTma>(U::kChunks * lane + j);
         if (kBF16) {  // the high halves of fp32 pairs
           const float* h = v + 8 * j;
           sts128(a, __byte_perm(__float_as_uint(h[0]), __float_as_uint(h[1]), 0x7632),
@@ -465,20 +522,44 @@ __global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
                  __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
         }
       }
-      __syncwarp();
+      if (kTma) {
+        fence_proxy_async_smem();  // each lane's writes, before the async-proxy read
+        __syncwarp();
+        const int64_t row0 = bu * U::kChunks / 8;  // bu is a multiple of 32
+        if (lane == 0) {
+          if (row0 < rows_y) {
+            const int64_t nrows = rows_y - row0 < U::kRows ? rows_y - row0 : U::kRows;
+            if (in_buf(y + row0 * 8, 128 * nrows, y, 16ull * npieces, &g_mx9_status))
+              tma_store_2d(&tm_y, 0, static_cast<int32_t>(row0), st);
+          }
+          bulk_commit();
+        }
+        // pieces past the last whole row: lane stores
 #pragma unroll
-      for (int r = 0; r < U::kChunks; ++r) {
-        const int c = 32 * r + lane;
-        const uint4 o = lds128(st + 16u * unpack_slot<kBF16>(c));
-        const int64_t piece = bu * U::kChunks + c;
-        if (bu + c / U::kChunks < nb &&
-            in_buf(y + piece, 16, y, 16ull * U::kChunks * nb, &g_mx9_status))
-          __stcs(y + piece, o);
+        for (int r = 0; r < U::kChunks; ++r) {
+          const int c = 32 * r + lane;
+          const int64_t piece = bu * U::kChunks + c;
+          if (piece >= 8 * rows_y && piece < npieces &&
+              in_buf(y + piece, 16, y, 16ull * npieces, &g_mx9_status))
+            __stcs(y + piece, lds128(st + 16u * unpack_slot<kBF16, kTma>(c)));
+        }
+      } else {
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < U::kChunks; ++r) {
+          const int c = 32 * r + lane;
+          const uint4 o = lds128(st + 16u * unpack_slot<kBF16, kTma>(c));
+          const int64_t piece = bu * U::kChunks + c;
+          if (piece < npieces && in_buf(y + piece, 16, y, 16ull * npieces, &g_mx9_status))
+            __stcs(y + piece, o);
+        }
+        __syncwarp();  // the buffer is rewritten by the next round
       }
-      __syncwarp();  // the buffer is rewritten by the next round
     }
   }
   pdl_trigger_at_end();
+  // the stores' reads of shared memory and their writes finish before exit
+  if (kTma && lane == 0) bulk_wait_all<0>();
 }
 
 // One full wave: as many resident blocks as the kernel's occupancy allows on
@@ -495,6 +576,60 @@ unsigned unpack_grid(Kernel kernel, int64_t nb, int group, int sms) {
   const int64_t want = (warps + kUnpackBlock / 32 - 1) / (kUnpackBlock / 32);
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<unsigned>(want < cap ? want : cap);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 unpack_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// The unpack's output as rows of 128 bytes (32 uint32 words), box `box_rows`
+// rows, 128-byte swizzle.  False when the driver cannot encode it.
+bool encode_unpack_map(CUtensorMap* map, void* y, int64_t rows_y, uint32_t box_rows) {
+  auto enc = unpack_map_encoder();
+  if (!enc || rows_y < 1 || rows_y > INT32_MAX) return false;  // row coordinates are int32
+  const cuuint64_t dims[2] = {32, static_cast<cuuint64_t>(rows_y)};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {32, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, y, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kBF16>
+cudaError_t launch_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t* prime, void* y,
+                          int64_t nb, int sms, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kUnpackBlock);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
+  const uint4* q16 = reinterpret_cast<const uint4*>(q);
+  uint4* y16 = static_cast<uint4*>(y);
+  CUtensorMap tm_y{};
+  const int64_t rows_y = nb * (kBF16 ? 32 : 64) / 128;
+  if constexpr ((kBF16 ? MXQ_MX9_UNPACK_TMA_BF16 : MXQ_MX9_UNPACK_TMA_F32) != 0) {
+    if (encode_unpack_map(&tm_y, y, rows_y, UnpackShape<kBF16, true>::kRows)) {
+      cfg.gridDim = dim3(unpack_grid(mx9_unpack_kernel<kBF16, true>, nb,
+                                     UnpackShape<kBF16, true>::kGroup, sms));
+      return cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<kBF16, true>, tm_y, q16, max_exp, prime,
+                                y16, nb, rows_y);
+    }
+  }
+  // lane stores: the output type's form, or tensors under 128 bytes
+  cfg.gridDim = dim3(unpack_grid(mx9_unpack_kernel<kBF16, false>, nb,
+                                 UnpackShape<kBF16, false>::kGroup, sms));
+  return cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<kBF16, false>, tm_y, q16, max_exp, prime, y16,
+                            nb, int64_t{0});
 }
 
 int check_dims(int dtype, int64_t rows, int64_t cols) {
@@ -609,19 +744,8 @@ extern "C" int mx9_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
   if (sms <= 0) return MXQ_ECUDA;
 
   const int64_t nb = n / 16;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(dtype == MXQ_F32
-                         ? unpack_grid(mx9_unpack_kernel<false>, nb, UnpackShape<false>::kGroup, sms)
-                         : unpack_grid(mx9_unpack_kernel<true>, nb, UnpackShape<true>::kGroup, sms));
-  cfg.blockDim = dim3(kUnpackBlock);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  allow_programmatic_launch(&cfg, &attr);
-  const uint4* q16 = reinterpret_cast<const uint4*>(q);
-  uint4* y16 = static_cast<uint4*>(y);
-  const cudaError_t e =
-      dtype == MXQ_F32
-          ? cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<false>, q16, max_exp, prime, y16, nb)
-          : cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<true>, q16, max_exp, prime, y16, nb);
+  const cudaError_t e = dtype == MXQ_F32
+                            ? launch_unpack<false>(q, max_exp, prime, y, nb, sms, stream)
+                            : launch_unpack<true>(q, max_exp, prime, y, nb, sms, stream);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }

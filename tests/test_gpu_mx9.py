@@ -180,3 +180,16 @@ def test_random_shapes(i):
     if i % 2:
         x = W.f32_to_bf16_bits(x)
     _check_pack_unpack(x, tag=f"case {i}: {rows}x{cols} {'bf16' if i % 2 else 'f32'} ")
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (1, 32), (1, 48), (3, 48), (5, 80), (999, 48),
+                                       (1000, 48), (4099, 4112)])
+def test_unpack_output_tails(rows, cols):
+    """The unpack stores whole 128-byte rows of output by tensor store and the
+    bytes past the last whole row by lane stores (under 128 bytes: all of
+    them).  These shapes leave 0, 32, 64 or 96 bytes past the last whole row
+    for fp32 and bf16 output, from a 64-byte tensor up to one whose rounds
+    wrap the grid several times; every byte is the oracle's."""
+    nz = min(16, rows * cols // 16 // 8)
+    x = W.mx9_outliers(rows, cols, seed=rows + cols, zero_blocks=nz, tiny_blocks=nz)
+    _check_pack_unpack(x, tag=f"{rows}x{cols} ")
