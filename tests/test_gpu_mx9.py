@@ -193,3 +193,27 @@ def test_unpack_output_tails(rows, cols):
     nz = min(16, rows * cols // 16 // 8)
     x = W.mx9_outliers(rows, cols, seed=rows + cols, zero_blocks=nz, tiny_blocks=nz)
     _check_pack_unpack(x, tag=f"{rows}x{cols} ")
+
+
+@pytest.mark.parametrize("offset_bytes", [16, 48, 112])
+def test_unpack_into_an_output_at_a_16_byte_offset(offset_bytes):
+    """The output may start at any 16-byte boundary (the tensor store's map is
+    encoded on the pointer as given): an output view 16, 48 or 112 bytes into
+    a larger buffer gets the oracle's bytes and nothing outside the view is
+    written."""
+    rows, cols = 129, 4096
+    x = W.mx9_outliers(rows, cols, seed=offset_bytes, zero_blocks=8, tiny_blocks=8)
+    q, e, p = mxq.mx9_pack(_dev(x))
+    rq, re, rp = oracle.mx9_pack(x)
+    for out_dtype, name, esize in ((torch.float32, "f32", 4), (torch.bfloat16, "bf16", 2)):
+        n = rows * cols
+        pad = offset_bytes // esize
+        big = _fill_like((n + pad + 64,), out_dtype)
+        y = big[pad:pad + n].view(rows, cols)
+        mxq.mx9_unpack(q, e, p, out_dtype, (rows, cols), out=y)
+        ry = oracle.mx9_unpack(rq, re, rp, name, rows, cols)
+        torch.cuda.synchronize()
+        raw = big.cpu().view(torch.uint8).numpy()
+        lo, hi = offset_bytes, offset_bytes + n * esize
+        assert_bytes_equal(raw[lo:hi], ry.view(np.uint8).reshape(-1), f"offset {offset_bytes} {name}")
+        assert (raw[:lo] == 0xAB).all() and (raw[hi:] == 0xAB).all(), "bytes outside the view"
