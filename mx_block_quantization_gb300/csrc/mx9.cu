@@ -578,33 +578,6 @@ unsigned unpack_grid(Kernel kernel, int64_t nb, int group, int sms) {
   return static_cast<unsigned>(want < cap ? want : cap);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 unpack_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// The unpack's output as rows of 128 bytes (32 uint32 words), box `box_rows`
-// rows, 128-byte swizzle.  False when the driver cannot encode it.
-bool encode_unpack_map(CUtensorMap* map, void* y, int64_t rows_y, uint32_t box_rows) {
-  auto enc = unpack_map_encoder();
-  if (!enc || rows_y < 1 || rows_y > INT32_MAX) return false;  // row coordinates are int32
-  const cuuint64_t dims[2] = {32, static_cast<cuuint64_t>(rows_y)};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {32, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, y, dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool kBF16>
 cudaError_t launch_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t* prime, void* y,
                           int64_t nb, int sms, cudaStream_t stream) {
@@ -618,7 +591,7 @@ cudaError_t launch_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
   CUtensorMap tm_y{};
   const int64_t rows_y = nb * (kBF16 ? 32 : 64) / 128;
   if constexpr ((kBF16 ? MXQ_MX9_UNPACK_TMA_BF16 : MXQ_MX9_UNPACK_TMA_F32) != 0) {
-    if (encode_unpack_map(&tm_y, y, rows_y, UnpackShape<kBF16, true>::kRows)) {
+    if (encode_rows128_map(&tm_y, y, rows_y, UnpackShape<kBF16, true>::kRows)) {
       cfg.gridDim = dim3(unpack_grid(mx9_unpack_kernel<kBF16, true>, nb,
                                      UnpackShape<kBF16, true>::kGroup, sms));
       return cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<kBF16, true>, tm_y, q16, max_exp, prime,
