@@ -107,9 +107,10 @@ using namespace mxq;
 // Unpack stores, per output type: 1 = each warp's decoded round leaves
 // shared memory as one tensor store (TMA) of whole 128-byte rows, 0 = lane
 // stores of 16 bytes.  Measured on GB300 at 16384x8192 and 32768x16384: the
-// tensor store is 2-5% faster for fp32 (2 KB per round) and 7-9% slower for
-// bf16 (1 KB per round, at 64 or 80 registers alike); 3 slots for fp32, or
-// unrolling 1 or 4 rounds, or 5 blocks per SM were all slower.
+// tensor store is 2-5% faster for fp32 (2 KB per round) and slower for bf16:
+// 7-9% with 1 KB rounds (at 64 or 80 registers alike), 1-2% with two blocks
+// per lane in 2 KB rounds; 3 slots for fp32, or unrolling 1 or 4 rounds, or
+// 5 blocks per SM were all slower.
 #ifndef MXQ_MX9_UNPACK_TMA_F32
 #define MXQ_MX9_UNPACK_TMA_F32 1
 #endif

@@ -315,6 +315,17 @@ constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight p
 #ifndef MXQ_REC_UNPACK_TMA
 #define MXQ_REC_UNPACK_TMA 1
 #endif
+// Minimum resident blocks per SM asked of the register allocator for the
+// tensor-store form (0: none), and whether its launch asks for the largest
+// shared-memory carveout.  Measured at 16384x8192 and 32768x16384: 3 or 4
+// blocks per SM (80 or 64 registers instead of 112-128, no spills) were 3-9%
+// slower, the carveout within 0.5%.
+#ifndef MXQ_REC_UNPACK_TMA_MINB
+#define MXQ_REC_UNPACK_TMA_MINB 0
+#endif
+#ifndef MXQ_REC_UNPACK_TMA_CARVEOUT
+#define MXQ_REC_UNPACK_TMA_CARVEOUT 0
+#endif
 constexpr int kRecSlots = 2;                  // staged runs per warp (tensor-store form)
 constexpr uint32_t kRecSlotBytes = 32u * 64u;  // one run of fp32 output
 constexpr uint32_t kRecTmaSmem = kWarps * kRecSlots * kRecSlotBytes + 1024u;  // + alignment
@@ -338,7 +349,7 @@ __host__ __device__ constexpr bool rec_tma() { return MXQ_REC_UNPACK_TMA && !kBF
 // store; the bytes past the last whole row (a trailing odd record's 64) by
 // lane stores.
 template <bool kBF16, int kFmt, bool kFlat>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFlat>() ? MXQ_REC_UNPACK_TMA_MINB : 0)
     mx_unpack_records_kernel(const __grid_constant__ CUtensorMap tm_y,
                              const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
                              int64_t ld, uint8_t* __restrict__ y, int64_t rows_y) {
@@ -1155,6 +1166,10 @@ int launch_records(int64_t nb, int64_t nbl, int64_t pitch, const uint8_t* packed
       if (!allowed[dev]) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kRecTmaSmem)) != cudaSuccess)
+          return MXQ_ECUDA;
+        if (MXQ_REC_UNPACK_TMA_CARVEOUT &&
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
           return MXQ_ECUDA;
         allowed[dev] = true;
       }
