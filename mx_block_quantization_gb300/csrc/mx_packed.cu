@@ -310,15 +310,19 @@ __device__ __forceinline__ float small_int_float(int32_t q) {
 #endif
 constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight per warp
 
-// fp32 output of contiguous rows: 1 = each run of 32 records (2 KB of output)
-// leaves shared memory as one tensor store (TMA), 0 = lane stores.
+// MX9 records to fp32 output of contiguous rows: 1 = each run of 32 records
+// (2 KB of output) leaves shared memory as one tensor store (TMA), 0 = lane
+// stores.  Measured (one box, graph replay, 16384x8192 / 32768x16384): MX9
+// fp32 0.950 / 0.970 of measured against 0.946 / 0.943; the same form for MX6
+// fp32 was slower (0.890 / 0.932 against 0.953 / 0.962), so MX6, bf16 output
+// and strided rows keep the lane stores.
 #ifndef MXQ_REC_UNPACK_TMA
 #define MXQ_REC_UNPACK_TMA 1
 #endif
 // Minimum resident blocks per SM asked of the register allocator for the
 // tensor-store form (0: none), and whether its launch asks for the largest
 // shared-memory carveout.  Measured at 16384x8192 and 32768x16384: 3 or 4
-// blocks per SM (80 or 64 registers instead of 112-128, no spills) were 3-9%
+// blocks per SM (80 or 64 registers instead of 128, no spills) were 1-8%
 // slower, the carveout within 0.5%.
 #ifndef MXQ_REC_UNPACK_TMA_MINB
 #define MXQ_REC_UNPACK_TMA_MINB 0
@@ -330,8 +334,10 @@ constexpr int kRecSlots = 2;                  // staged runs per warp (tensor-st
 constexpr uint32_t kRecSlotBytes = 32u * 64u;  // one run of fp32 output
 constexpr uint32_t kRecTmaSmem = kWarps * kRecSlots * kRecSlotBytes + 1024u;  // + alignment
 
-template <bool kBF16, bool kFlat>
-__host__ __device__ constexpr bool rec_tma() { return MXQ_REC_UNPACK_TMA && !kBF16 && kFlat; }
+template <bool kBF16, int kFmt, bool kFlat>
+__host__ __device__ constexpr bool rec_tma() {
+  return MXQ_REC_UNPACK_TMA && !kBF16 && kFmt == MXQ_FMT_MX9 && kFlat;
+}
 
 // Unpack of a contiguous tensor blocked along its rows: nb records, the
 // output is nb * 16 elements in rows of nbl blocks, ld elements apart (ld ==
@@ -342,18 +348,18 @@ __host__ __device__ constexpr bool rec_tma() { return MXQ_REC_UNPACK_TMA && !kBF
 // output bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp
 // cover 512 contiguous bytes.  packed and y are 16-byte aligned.  kFlat: the
 // rows follow each other (ld == 16 nbl); a separate instantiation so that
-// the strided form's row bases cost the flat one no registers.  fp32 output
-// of contiguous rows (rec_tma): the 16-byte units of a run of 32 records go
+// the strided form's row bases cost the flat one no registers.  MX9 to fp32
+// output of contiguous rows (rec_tma): the 16-byte units of a run of 32 records go
 // to a per-warp staging slot laid out with the 128-byte swizzle of tm_y (the
 // output as rows_y rows of 128 bytes), and the run leaves as one tensor
 // store; the bytes past the last whole row (a trailing odd record's 64) by
 // lane stores.
 template <bool kBF16, int kFmt, bool kFlat>
-__global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFlat>() ? MXQ_REC_UNPACK_TMA_MINB : 0)
+__global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_REC_UNPACK_TMA_MINB : 0)
     mx_unpack_records_kernel(const __grid_constant__ CUtensorMap tm_y,
                              const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
                              int64_t ld, uint8_t* __restrict__ y, int64_t rows_y) {
-  constexpr bool kTma = rec_tma<kBF16, kFlat>();
+  constexpr bool kTma = rec_tma<kBF16, kFmt, kFlat>();
   extern __shared__ uint8_t rec_dyn[];  // tensor-store form: kWarps x kRecSlots runs
   uint32_t ost = 0;
   if (kTma) {
@@ -1141,8 +1147,7 @@ int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
 }
 
 // The record unpack over nb records (rows of nbl blocks, pitch elements
-// apart): one thread per kRecRuns records, capped at a full wave of resident
-// blocks.  The fp32 contiguous form also gets the tensor map of its output and
+// apart): one thread per kRecRuns records, capped at 8 blocks per SM.  The fp32 contiguous form also gets the tensor map of its output and
 // its staging slots in dynamic shared memory (lane stores alone when the map
 // cannot be encoded: rows_y = 0).
 template <bool kBF16, int kFmt, bool kFlat>
@@ -1154,7 +1159,7 @@ int launch_records(int64_t nb, int64_t nbl, int64_t pitch, const uint8_t* packed
   CUtensorMap tm_y{};
   int64_t rows_y = 0;
   size_t dyn = 0;
-  if constexpr (rec_tma<kBF16, kFlat>()) {
+  if constexpr (rec_tma<kBF16, kFmt, kFlat>()) {
     // with the static record stage the block uses more than 48 KB of shared
     // memory, which each device's context must allow once per kernel
     static std::mutex mu;
@@ -1178,13 +1183,11 @@ int launch_records(int64_t nb, int64_t nbl, int64_t pitch, const uint8_t* packed
     rows_y = nb / 2;  // 64 output bytes per record
     if (!encode_rows128_map(&tm_y, y, rows_y, 16)) rows_y = 0;
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, dyn) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  // as many blocks as 8 per SM, whatever fits at once: measured faster than
+  // one persistent wave of resident blocks (3-6% on every record unpack)
   const int64_t items = (nb + kRecRuns - 1) / kRecRuns;
   const int64_t want = (items + kThreads - 1) / kThreads;
-  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kThreads);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
   cfg.blockDim = dim3(kThreads);
