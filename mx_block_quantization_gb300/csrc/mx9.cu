@@ -25,8 +25,6 @@
 // instructions) into a per-warp shared-memory stage, from which a warp's
 // round of 32 blocks leaves as one tensor store (fp32 output) or as 512-byte
 // contiguous lane stores (bf16 output).
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -75,6 +73,21 @@ using namespace mxq;
 #ifndef MXQ_MX9_PACK_CTAS_PER_SM
 #define MXQ_MX9_PACK_CTAS_PER_SM 2
 #endif
+// Waves of resident blocks in the pack's grid (1: one persistent wave; more
+// only where every block still gets MXQ_MX9_PACK_MIN_STAGES stages).
+// Measured at 16384x8192 / 32768x16384 (fraction of the measured copy
+// rate): the split bf16 pack 0.987 / 0.955 with one wave, 0.983-0.999 /
+// 1.028-1.031 with 16; every other form was fastest with one (16 waves: split
+// fp32 equal, records 9-21% slower; a block per stage: 20-50% slower).
+#ifndef MXQ_MX9_PACK_WAVES_SPLIT_BF16
+#define MXQ_MX9_PACK_WAVES_SPLIT_BF16 16
+#endif
+#ifndef MXQ_MX9_PACK_WAVES
+#define MXQ_MX9_PACK_WAVES 1
+#endif
+#ifndef MXQ_MX9_PACK_MIN_STAGES
+#define MXQ_MX9_PACK_MIN_STAGES 3
+#endif
 #ifndef MXQ_MX9_PACK_BF16_PER_THREAD
 #define MXQ_MX9_PACK_BF16_PER_THREAD 2
 #endif
@@ -87,50 +100,15 @@ using namespace mxq;
 #ifndef MXQ_MX9_UNPACK_PRMT_BF16
 #define MXQ_MX9_UNPACK_PRMT_BF16 1
 #endif
+// Rounds of 32 blocks a warp of the unpack decodes (its loads all issued
+// before the first decode).  Measured with the grid below at 16384x8192 and
+// 32768x16384: fp32 1 or 2 alike (1.04-1.05 of the measured copy rate), 4
+// slower; bf16 2 best (1.045-1.067), 4 and 8 slower.
 #ifndef MXQ_MX9_UNPACK_UNROLL_F32
-#define MXQ_MX9_UNPACK_UNROLL_F32 2
+#define MXQ_MX9_UNPACK_UNROLL_F32 1
 #endif
 #ifndef MXQ_MX9_UNPACK_UNROLL_BF16
-#define MXQ_MX9_UNPACK_UNROLL_BF16 4
-#endif
-
-// Unpack round order: 1 = each warp takes kUnroll adjacent rounds of 32
-// blocks, 2 = grid-wide rounds (round u of all warps adjacent, so the grid
-// writes one contiguous stretch at a time).  2 measured best inside the bench
-// step; a former kernel with a lane per 16 output bytes (four lanes sharing a
-// block, each loading its exponent and prime bytes) was 3% faster back to
-// back but 1-2% slower in the step, after the pack or the dual cast.
-#ifndef MXQ_MX9_UNPACK_KIND
-#define MXQ_MX9_UNPACK_KIND 2
-#endif
-
-// Unpack stores, per output type: 1 = each warp's decoded round leaves
-// shared memory as one tensor store (TMA) of whole 128-byte rows, 0 = lane
-// stores of 16 bytes.  Measured on GB300 at 16384x8192 and 32768x16384: the
-// tensor store is 2-5% faster for fp32 (2 KB per round) and slower for bf16:
-// 7-9% with 1 KB rounds (at 64 or 80 registers alike), 1-2% with two blocks
-// per lane in 2 KB rounds; 3 slots for fp32, or unrolling 1 or 4 rounds, or
-// 5 blocks per SM were all slower.
-#ifndef MXQ_MX9_UNPACK_TMA_F32
-#define MXQ_MX9_UNPACK_TMA_F32 1
-#endif
-#ifndef MXQ_MX9_UNPACK_TMA_BF16
-#define MXQ_MX9_UNPACK_TMA_BF16 0
-#endif
-// Minimum resident blocks per SM asked of the register allocator (0: none).
-#ifndef MXQ_MX9_UNPACK_MINB_F32
-#define MXQ_MX9_UNPACK_MINB_F32 0
-#endif
-#ifndef MXQ_MX9_UNPACK_MINB_BF16
-#define MXQ_MX9_UNPACK_MINB_BF16 0
-#endif
-// Staging slots per warp for the tensor-store form (a slot is rewritten once
-// the store issued from it kSlots rounds earlier has read it).
-#ifndef MXQ_MX9_UNPACK_SLOTS_F32
-#define MXQ_MX9_UNPACK_SLOTS_F32 2
-#endif
-#ifndef MXQ_MX9_UNPACK_SLOTS_BF16
-#define MXQ_MX9_UNPACK_SLOTS_BF16 4
+#define MXQ_MX9_UNPACK_UNROLL_BF16 2
 #endif
 
 constexpr int kUnpackBlock = 256;
@@ -165,6 +143,8 @@ struct PackShape {
                       : (kBF16 ? MXQ_MX9_REC_BF16_RING_KB : MXQ_MX9_REC_F32_RING_KB)) *
       1024u;
   static constexpr int kStages = static_cast<int>(kRingBytes / kStageBytes);
+  static constexpr int kWaves =
+      kOut == kSplit && kBF16 ? MXQ_MX9_PACK_WAVES_SPLIT_BF16 : MXQ_MX9_PACK_WAVES;
   static constexpr uint32_t kRecord =
       kOut == kRecMx9 ? MXQ_MX9_RECORD_BYTES : kOut == kRecMx6 ? MXQ_MX6_RECORD_BYTES : 0u;
   static constexpr uint32_t kOffBar = kStages * kStageBytes;
@@ -382,37 +362,31 @@ __device__ __forceinline__ float small_int_to_float(int32_t q) {
 // Unpack: a lane decodes whole 16-element blocks, one per round: one 16-byte
 // load of q plus the block's own exponent and prime bytes (a warp's loads of a
 // round are 512 contiguous q bytes and 32 contiguous bytes of each of the
-// others), kUnroll rounds' loads issued before the first decode.  The decoded
-// block (64 bytes of fp32 or 32 of bf16) goes to a per-warp staging buffer in
-// shared memory, from which the round's 32 blocks (2 KB fp32, 1 KB bf16, one
-// contiguous stretch of the output) leave either as one tensor store (TMA)
-// or as lane stores of 16-byte pieces, every instruction writing 512
-// contiguous bytes.  q * 2^k is exact (|q| <= 127, k >= -126) except for
-// overflow in max_exp 255 blocks; a bf16 result has at most 7 significant
-// bits, so the top half of the fp32 is the exact bf16.
-template <bool kBF16, bool kTma>
+// others), the loads of all kUnroll rounds issued before the first decode.
+// The decoded block (64 bytes of fp32 or 32 of bf16) goes to a per-warp
+// staging buffer in shared memory, from which each lane stores 16-byte pieces
+// so that every store instruction writes 512 contiguous output bytes.  A warp
+// takes kUnroll consecutive rounds and the grid has a warp for every group of
+// them: blocks are scheduled as earlier ones leave, which measured 10-15%
+// faster than one persistent wave of resident blocks walking the tensor.
+// q * 2^k is exact (|q| <= 127, k >= -126) except for overflow in max_exp
+// 255 blocks; a bf16 result has at most 7 significant bits, so the top half
+// of the fp32 is the exact bf16.
+template <bool kBF16>
 struct UnpackShape {
   static constexpr int kChunks = kBF16 ? 2 : 4;  // 16-byte output pieces per block
   static constexpr int kUnroll = kBF16 ? MXQ_MX9_UNPACK_UNROLL_BF16 : MXQ_MX9_UNPACK_UNROLL_F32;
   static constexpr int kWarps = kUnpackBlock / 32;
-  static constexpr int kGroup = 32 * kUnroll;                   // blocks per warp iteration
+  static constexpr int kGroup = 32 * kUnroll;                   // blocks per warp
   static constexpr uint32_t kStageBytes = 32u * kChunks * 16u;  // one round of a warp
-  static constexpr int kRows = 32 * kChunks / 8;                // 128-byte output rows per round
-  static constexpr int kSlots =
-      kTma ? (kBF16 ? MXQ_MX9_UNPACK_SLOTS_BF16 : MXQ_MX9_UNPACK_SLOTS_F32) : 1;
-  static_assert(kStageBytes % 1024 == 0, "a slot keeps the 1024-byte swizzle period");
 };
 
 // Slot of output piece c (piece c % kChunks of the round's block c / kChunks)
-// in a warp's staging buffer.  Lane stores: XOR-ing bits 3.. of c into its
-// low bits makes both access patterns conflict-free: the writes, where lane l
-// stores the pieces of its own block, and the reads, where lane l loads piece
-// 32r + l.  Tensor store: the 128-byte swizzle of the tensor map (16-byte
-// column c % 8 of 128-byte row c / 8 sits at column (c % 8) ^ (row % 8)),
-// under which the writes are conflict-free as well.
-template <bool kBF16, bool kTma>
+// in a warp's staging buffer.  XOR-ing bits 3.. of c into its low bits makes
+// both access patterns conflict-free: the writes, where lane l stores the
+// pieces of its own block, and the reads, where lane l loads piece 32r + l.
+template <bool kBF16>
 __device__ __forceinline__ uint32_t unpack_slot(int c) {
-  if (kTma) return static_cast<uint32_t>((c & ~7) | ((c ^ (c >> 3)) & 7));
   return static_cast<uint32_t>(kBF16 ? c ^ ((c >> 3) & 1) : c ^ ((c >> 3) & 3));
 }
 
@@ -437,40 +411,26 @@ __device__ __forceinline__ void unpack4_biased(uint32_t vx, float s0, float s1, 
   y[3] = fmul_rn_noftz(fadd_rn_noftz(__uint_as_float(__byte_perm(vx, 0x4B000000u, 0x7653)), -kBias), s1);
 }
 
-// tm_y (tensor-store form only) views the output as `rows_y` rows of 128
-// bytes (32 uint32 words), box kRows rows, 128-byte swizzle; the bytes past
-// the last whole row (under 128) are written by lane stores.
-template <bool kBF16, bool kTma>
-__global__ void __launch_bounds__(kUnpackBlock,
-                                  kBF16 ? MXQ_MX9_UNPACK_MINB_BF16 : MXQ_MX9_UNPACK_MINB_F32)
-    mx9_unpack_kernel(
-    const __grid_constant__ CUtensorMap tm_y, const uint4* __restrict__ q,
-    const uint8_t* __restrict__ max_exp, const uint8_t* __restrict__ prime,
-    uint4* __restrict__ y, int64_t nb, int64_t rows_y) {
-  using U = UnpackShape<kBF16, kTma>;
-  __shared__ __align__(1024) uint8_t stage[U::kWarps][U::kSlots][U::kStageBytes];
-  if (kTma && threadIdx.x == 0) tma_prefetch_desc(&tm_y);
+template <bool kBF16>
+__global__ void __launch_bounds__(kUnpackBlock) mx9_unpack_kernel(
+    const uint4* __restrict__ q, const uint8_t* __restrict__ max_exp,
+    const uint8_t* __restrict__ prime, uint4* __restrict__ y, int64_t nb) {
+  using U = UnpackShape<kBF16>;
+  __shared__ __align__(16) uint8_t stage[U::kWarps][U::kStageBytes];
   pdl_wait();
   pdl_trigger_at_start();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t st = smem_u32(stage[warp]);
   const int64_t gwarps = static_cast<int64_t>(gridDim.x) * U::kWarps;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * U::kWarps + warp;
-  const int64_t npieces = nb * U::kChunks;
-  // the swizzle assumes 1024-byte aligned slots; were the array placed
-  // otherwise, every piece would leave by lane stores instead
-  if (kTma && (smem_u32(stage) & 1023u) != 0) rows_y = 0;
-  // first block of round u of iteration it: a warp's own group of kUnroll
-  // rounds, or grid-wide rounds (all warps' round u adjacent)
-  auto round_base = [&](int64_t it, int u) -> int64_t {
-    return MXQ_MX9_UNPACK_KIND == 2 ? ((it * U::kUnroll + u) * gwarps + gw) * 32
-                                    : (it * gwarps + gw) * U::kGroup + 32 * u;
-  };
-  for (int64_t it = 0; round_base(it, 0) < nb; ++it) {
+  // warp gw takes groups gw, gw + gwarps, ... (one group when the grid covers
+  // the tensor, as launched)
+  for (int64_t g0 = (static_cast<int64_t>(blockIdx.x) * U::kWarps + warp) * U::kGroup; g0 < nb;
+       g0 += gwarps * U::kGroup) {
     uint4 qv[U::kUnroll];
     uint32_t ev[U::kUnroll], pv[U::kUnroll];
 #pragma unroll
     for (int u = 0; u < U::kUnroll; ++u) {
-      const int64_t b = round_base(it, u) + lane;
+      const int64_t b = g0 + 32 * u + lane;
       qv[u] = make_uint4(0u, 0u, 0u, 0u);
       ev[u] = pv[u] = 0u;
       if (b < nb && in_buf(q + b, 16, q, 16ull * nb, &g_mx9_status) &&
@@ -483,15 +443,8 @@ __global__ void __launch_bounds__(kUnpackBlock,
     }
 #pragma unroll
     for (int u = 0; u < U::kUnroll; ++u) {
-      const int64_t bu = round_base(it, u);  // first block of the round (warp-uniform)
+      const int64_t bu = g0 + 32 * u;  // first block of the round (warp-uniform)
       if (bu >= nb) break;
-      const uint32_t st =
-          smem_u32(stage[warp][kTma ? static_cast<int>((it * U::kUnroll + u) % U::kSlots) : 0]);
-      if (kTma) {
-        // the store issued from this slot kSlots rounds ago has read it
-        if (lane == 0) bulk_wait_read<U::kSlots - 1>();
-        __syncwarp();
-      }
       const int E = static_cast<int>(ev[u]) - 127;
       const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
       float v[16];  // word k holds elements 4k..4k+3, i.e. pairs 2k and 2k+1
@@ -511,7 +464,7 @@ __global__ void __launch_bounds__(kUnpackBlock,
       }
 #pragma unroll
       for (int j = 0; j < U::kChunks; ++j) {
-        const uint32_t a = st + 16u * unpack_slot<kBF16, kTma>(U::kChunks * lane + j);
+        const uint32_t a = st + 16u * unpack_slot<kBF16>(U::kChunks * lane + j);
         if (kBF16) {  // the high halves of fp32 pairs
           const float* h = v + 8 * j;
           sts128(a, __byte_perm(__float_as_uint(h[0]), __float_as_uint(h[1]), 0x7632),
@@ -523,87 +476,29 @@ __global__ void __launch_bounds__(kUnpackBlock,
                  __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
         }
       }
-      if (kTma) {
-        fence_proxy_async_smem();  // each lane's writes, before the async-proxy read
-        __syncwarp();
-        const int64_t row0 = bu * U::kChunks / 8;  // bu is a multiple of 32
-        if (lane == 0) {
-          if (row0 < rows_y) {
-            const int64_t nrows = rows_y - row0 < U::kRows ? rows_y - row0 : U::kRows;
-            if (in_buf(y + row0 * 8, 128 * nrows, y, 16ull * npieces, &g_mx9_status))
-              tma_store_2d(&tm_y, 0, static_cast<int32_t>(row0), st);
-          }
-          bulk_commit();
-        }
-        // pieces past the last whole row: lane stores
+      __syncwarp();
 #pragma unroll
-        for (int r = 0; r < U::kChunks; ++r) {
-          const int c = 32 * r + lane;
-          const int64_t piece = bu * U::kChunks + c;
-          if (piece >= 8 * rows_y && piece < npieces &&
-              in_buf(y + piece, 16, y, 16ull * npieces, &g_mx9_status))
-            __stcs(y + piece, lds128(st + 16u * unpack_slot<kBF16, kTma>(c)));
-        }
-      } else {
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < U::kChunks; ++r) {
-          const int c = 32 * r + lane;
-          const uint4 o = lds128(st + 16u * unpack_slot<kBF16, kTma>(c));
-          const int64_t piece = bu * U::kChunks + c;
-          if (piece < npieces && in_buf(y + piece, 16, y, 16ull * npieces, &g_mx9_status))
-            __stcs(y + piece, o);
-        }
-        __syncwarp();  // the buffer is rewritten by the next round
+      for (int r = 0; r < U::kChunks; ++r) {
+        const int c = 32 * r + lane;
+        const uint4 o = lds128(st + 16u * unpack_slot<kBF16>(c));
+        const int64_t piece = bu * U::kChunks + c;
+        if (bu + c / U::kChunks < nb &&
+            in_buf(y + piece, 16, y, 16ull * U::kChunks * nb, &g_mx9_status))
+          __stcs(y + piece, o);
       }
+      __syncwarp();  // the buffer is rewritten by the next round
     }
   }
   pdl_trigger_at_end();
-  // the stores' reads of shared memory and their writes finish before exit
-  if (kTma && lane == 0) bulk_wait_all<0>();
 }
 
-// One full wave: as many resident blocks as the kernel's occupancy allows on
-// every SM, or fewer when the problem is small (one warp per group of
-// `group` 16-element blocks).
-template <typename Kernel>
-unsigned unpack_grid(Kernel kernel, int64_t nb, int group, int sms) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kUnpackBlock, 0) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const int64_t warps = (nb + group - 1) / group;
-  const int64_t want = (warps + kUnpackBlock / 32 - 1) / (kUnpackBlock / 32);
-  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
-  return static_cast<unsigned>(want < cap ? want : cap);
-}
-
+// A warp for every kGroup blocks (grid capped at the hardware's limit).
 template <bool kBF16>
-cudaError_t launch_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t* prime, void* y,
-                          int64_t nb, int sms, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kUnpackBlock);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  allow_programmatic_launch(&cfg, &attr);
-  const uint4* q16 = reinterpret_cast<const uint4*>(q);
-  uint4* y16 = static_cast<uint4*>(y);
-  CUtensorMap tm_y{};
-  const int64_t rows_y = nb * (kBF16 ? 32 : 64) / 128;
-  if constexpr ((kBF16 ? MXQ_MX9_UNPACK_TMA_BF16 : MXQ_MX9_UNPACK_TMA_F32) != 0) {
-    if (encode_rows128_map(&tm_y, y, rows_y, UnpackShape<kBF16, true>::kRows)) {
-      cfg.gridDim = dim3(unpack_grid(mx9_unpack_kernel<kBF16, true>, nb,
-                                     UnpackShape<kBF16, true>::kGroup, sms));
-      return cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<kBF16, true>, tm_y, q16, max_exp, prime,
-                                y16, nb, rows_y);
-    }
-  }
-  // lane stores: the output type's form, or tensors under 128 bytes
-  cfg.gridDim = dim3(unpack_grid(mx9_unpack_kernel<kBF16, false>, nb,
-                                 UnpackShape<kBF16, false>::kGroup, sms));
-  return cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<kBF16, false>, tm_y, q16, max_exp, prime, y16,
-                            nb, int64_t{0});
+unsigned unpack_grid(int64_t nb) {
+  using U = UnpackShape<kBF16>;
+  const int64_t warps = (nb + U::kGroup - 1) / U::kGroup;
+  const int64_t want = (warps + U::kWarps - 1) / U::kWarps;
+  return static_cast<unsigned>(want < INT32_MAX ? want : INT32_MAX);
 }
 
 int check_dims(int dtype, int64_t rows, int64_t cols) {
@@ -626,7 +521,13 @@ cudaError_t launch_pack(const void* x, int64_t nb, int64_t nbl, int64_t pitch, u
     attr_done[dev] = true;
   }
   const int64_t nchunks = (nb + S::kBlocksPerStage - 1) / S::kBlocksPerStage;
-  const int64_t cap = static_cast<int64_t>(sms) * MXQ_MX9_PACK_CTAS_PER_SM;
+  // one wave of resident blocks, or kWaves whole waves when every block then
+  // still gets MXQ_MX9_PACK_MIN_STAGES stages (its ring set-up amortized);
+  // a partial last wave measured slower (4096x4096 bf16: 0.80-0.93 against
+  // 0.97 for one wave)
+  const int64_t wave = static_cast<int64_t>(sms) * MXQ_MX9_PACK_CTAS_PER_SM;
+  const int64_t cap =
+      nchunks >= wave * S::kWaves * MXQ_MX9_PACK_MIN_STAGES ? wave * S::kWaves : wave;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nchunks < cap ? nchunks : cap));
   cfg.blockDim = dim3(S::kThreads);
@@ -714,12 +615,18 @@ extern "C" int mx9_unpack(const int8_t* q, const uint8_t* max_exp, const uint8_t
       {reinterpret_cast<uintptr_t>(prime), static_cast<uint64_t>(n / 16)},
   };
   if (ranges_overlap(r, 4)) return MXQ_EOVERLAP;
-  const int sms = sm_count_current_device(nullptr);
-  if (sms <= 0) return MXQ_ECUDA;
-
   const int64_t nb = n / 16;
-  const cudaError_t e = dtype == MXQ_F32
-                            ? launch_unpack<false>(q, max_exp, prime, y, nb, sms, stream)
-                            : launch_unpack<true>(q, max_exp, prime, y, nb, sms, stream);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dtype == MXQ_F32 ? unpack_grid<false>(nb) : unpack_grid<true>(nb));
+  cfg.blockDim = dim3(kUnpackBlock);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  allow_programmatic_launch(&cfg, &attr);
+  const uint4* q16 = reinterpret_cast<const uint4*>(q);
+  uint4* y16 = static_cast<uint4*>(y);
+  const cudaError_t e =
+      dtype == MXQ_F32
+          ? cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<false>, q16, max_exp, prime, y16, nb)
+          : cudaLaunchKernelEx(&cfg, mx9_unpack_kernel<true>, q16, max_exp, prime, y16, nb);
   return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
 }

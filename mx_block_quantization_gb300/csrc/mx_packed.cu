@@ -27,12 +27,8 @@
 //   unaligned pointers): the generic row kernels, one thread per block, a
 //   warp's 32 consecutive records staged in shared memory and moved with
 //   coalesced copies.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "mx_block.cuh"
 #include "mxq.h"
@@ -310,35 +306,6 @@ __device__ __forceinline__ float small_int_float(int32_t q) {
 #endif
 constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight per warp
 
-// MX9 records to fp32 output of contiguous rows: 1 = each run of 32 records
-// (2 KB of output) leaves shared memory as one tensor store (TMA), 0 = lane
-// stores.  Measured (one box, graph replay, 16384x8192 / 32768x16384): MX9
-// fp32 0.950 / 0.970 of measured against 0.946 / 0.943; the same form for MX6
-// fp32 was slower (0.890 / 0.932 against 0.953 / 0.962), so MX6, bf16 output
-// and strided rows keep the lane stores.
-#ifndef MXQ_REC_UNPACK_TMA
-#define MXQ_REC_UNPACK_TMA 1
-#endif
-// Minimum resident blocks per SM asked of the register allocator for the
-// tensor-store form (0: none), and whether its launch asks for the largest
-// shared-memory carveout.  Measured at 16384x8192 and 32768x16384: 3 or 4
-// blocks per SM (80 or 64 registers instead of 128, no spills) were 1-8%
-// slower, the carveout within 0.5%.
-#ifndef MXQ_REC_UNPACK_TMA_MINB
-#define MXQ_REC_UNPACK_TMA_MINB 0
-#endif
-#ifndef MXQ_REC_UNPACK_TMA_CARVEOUT
-#define MXQ_REC_UNPACK_TMA_CARVEOUT 0
-#endif
-constexpr int kRecSlots = 2;                  // staged runs per warp (tensor-store form)
-constexpr uint32_t kRecSlotBytes = 32u * 64u;  // one run of fp32 output
-constexpr uint32_t kRecTmaSmem = kWarps * kRecSlots * kRecSlotBytes + 1024u;  // + alignment
-
-template <bool kBF16, int kFmt, bool kFlat>
-__host__ __device__ constexpr bool rec_tma() {
-  return MXQ_REC_UNPACK_TMA && !kBF16 && kFmt == MXQ_FMT_MX9 && kFlat;
-}
-
 // Unpack of a contiguous tensor blocked along its rows: nb records, the
 // output is nb * 16 elements in rows of nbl blocks, ld elements apart (ld ==
 // 16 nbl: one flat run; otherwise nbl >= 32 kRecRuns, so that the records a
@@ -348,25 +315,11 @@ __host__ __device__ constexpr bool rec_tma() {
 // output bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp
 // cover 512 contiguous bytes.  packed and y are 16-byte aligned.  kFlat: the
 // rows follow each other (ld == 16 nbl); a separate instantiation so that
-// the strided form's row bases cost the flat one no registers.  MX9 to fp32
-// output of contiguous rows (rec_tma): the 16-byte units of a run of 32 records go
-// to a per-warp staging slot laid out with the 128-byte swizzle of tm_y (the
-// output as rows_y rows of 128 bytes), and the run leaves as one tensor
-// store; the bytes past the last whole row (a trailing odd record's 64) by
-// lane stores.
+// the strided form's row bases cost the flat one no registers.
 template <bool kBF16, int kFmt, bool kFlat>
-__global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_REC_UNPACK_TMA_MINB : 0)
-    mx_unpack_records_kernel(const __grid_constant__ CUtensorMap tm_y,
-                             const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
-                             int64_t ld, uint8_t* __restrict__ y, int64_t rows_y) {
-  constexpr bool kTma = rec_tma<kBF16, kFmt, kFlat>();
-  extern __shared__ uint8_t rec_dyn[];  // tensor-store form: kWarps x kRecSlots runs
-  uint32_t ost = 0;
-  if (kTma) {
-    if (threadIdx.x == 0) tma_prefetch_desc(&tm_y);
-    ost = ((smem_u32(rec_dyn) + 1023u) & ~1023u) +
-          static_cast<uint32_t>(threadIdx.x >> 5) * kRecSlots * kRecSlotBytes;
-  }
+__global__ void __launch_bounds__(kThreads)
+    mx_unpack_records_kernel(const uint8_t* __restrict__ packed, int64_t nb, int64_t nbl,
+                             int64_t ld, uint8_t* __restrict__ y) {
   pdl_wait();  // inputs may be the previous kernel's output
   pdl_trigger_at_start();
   constexpr int RB = Fmt<kFmt>::kRecord;
@@ -381,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_
   const int64_t ngroups = (nb + kGroup - 1) / kGroup;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kWarps;
   constexpr bool flat = kFlat;  // else rows of nbl >= kGroup blocks, ld elements apart
-  uint32_t runs = 0;  // tensor-store form: runs staged so far (slot = runs % kRecSlots)
   for (int64_t grp = static_cast<int64_t>(blockIdx.x) * kWarps + warp; grp < ngroups;
        grp += wstride) {
     const int64_t r0 = grp * kGroup;
@@ -418,14 +370,7 @@ __global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_
     for (int j = 0; j < kParts * kRecRuns; ++j) {
       const int u = j * 32 + lane;  // output unit of this group
       const int r = u / kParts, part = u % kParts;
-      // tensor-store form: a run is j = kParts * run .. kParts * run + kParts - 1
-      const uint32_t slot = ost + (runs % kRecSlots) * kRecSlotBytes;
-      if (kTma && j % kParts == 0) {
-        // the store issued from this slot kRecSlots runs ago has read it
-        if (lane == 0) bulk_wait_read<kRecSlots - 1>();
-        __syncwarp();
-      }
-      if (r < nvalid) {
+      if (r >= nvalid) continue;
       const uint32_t rec = st + static_cast<uint32_t>(r) * RB;
       uint32_t head, code[kElems];
       if (kFmt == MXQ_FMT_MX9) {
@@ -479,13 +424,6 @@ __global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_
           val[k] = fmul_rn_noftz(small_int_float(static_cast<int>(code[k] << 27) >> 27),
                                  (ubits >> (k >> 1)) & 1u ? s_dem : s_keep);
       }
-      if (kTma) {
-        // unit u % (32 kParts) of the run, at its swizzled place in the slot
-        const int c = u % (32 * kParts);
-        sts128(slot + 16u * static_cast<uint32_t>((c & ~7) | ((c ^ (c >> 3)) & 7)),
-               __float_as_uint(val[0]), __float_as_uint(val[1]), __float_as_uint(val[2]),
-               __float_as_uint(val[3]));
-      } else {
       // this 16-byte output unit (strided rows: from the group's two row bases,
       // measured +2 to +13% over per-unit row arithmetic; contiguous rows keep
       // the flat index, which measured 1-2% faster than the bases there)
@@ -495,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_
       // y spans (nb / nbl - 1) * ld + 16 nbl elements
       if (!in_buf(dst, 16, y, static_cast<uint64_t>((nb / nbl - 1) * ld + 16 * nbl) * kEsize,
                   &g_packed_status)) {
+        continue;
       } else if (kBF16) {
         uint32_t o[4];
 #pragma unroll
@@ -504,41 +443,9 @@ __global__ void __launch_bounds__(kThreads, rec_tma<kBF16, kFmt, kFlat>() ? MXQ_
       } else {
         __stcs(reinterpret_cast<float4*>(dst), make_float4(val[0], val[1], val[2], val[3]));
       }
-      }
-      }  // r < nvalid
-      if (kTma && j % kParts == kParts - 1) {
-        // the run is staged: one tensor store of its whole 128-byte rows (the
-        // map clips rows past the output), lane stores for the bytes past the
-        // last whole row, one bulk group per run (empty ones too, so that the
-        // slot waits above count runs)
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int64_t rec0 = r0 + 32 * (j / kParts);  // first record of the run
-        if (lane == 0) {
-          const int64_t row = rec0 / 2;  // 64 output bytes per record; rec0 is even
-          if (rec0 < nb && row < rows_y) {
-            const int64_t nrows = rows_y - row < 16 ? rows_y - row : 16;
-            if (in_buf(y + 128 * row, 128 * nrows, y, static_cast<uint64_t>(nb) * 64, &g_packed_status))
-              tma_store_2d(&tm_y, 0, static_cast<int32_t>(row), slot);
-          }
-          bulk_commit();
-        }
-#pragma unroll
-        for (int k = 0; k < kParts; ++k) {
-          const int c = 32 * k + lane;
-          const int64_t piece = rec0 * kParts + c;  // 16-byte piece of the output
-          if (piece >= 8 * rows_y && piece < nb * kParts &&
-              in_buf(y + 16 * piece, 16, y, static_cast<uint64_t>(nb) * 64, &g_packed_status))
-            __stcs(reinterpret_cast<uint4*>(y) + piece,
-                   lds128(slot + 16u * static_cast<uint32_t>((c & ~7) | ((c ^ (c >> 3)) & 7))));
-        }
-        ++runs;
-      }
     }
     __syncwarp();
   }
-  // the tensor stores' reads of shared memory and their writes finish before exit
-  if (kTma && lane == 0) bulk_wait_all<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -1130,13 +1037,14 @@ bool rows_ok(const void* p, int dtype, int64_t rows, int64_t cols, int64_t ld, i
   return ld == cols || rows == 1 || cols / 16 >= min_nbl;
 }
 
-// One thread per work item (capped at a full wave of 8 blocks per SM).
-template <typename Kernel, typename... Args>
+// One thread per work item: the whole grid (kWhole: blocks are scheduled as
+// earlier ones leave), or at most 8 blocks per SM that then walk the items.
+template <bool kWhole = false, typename Kernel, typename... Args>
 int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
   const int sms = sm_count_current_device(nullptr);
   if (sms <= 0) return MXQ_ECUDA;
   const int64_t want = (nb + kThreads - 1) / kThreads;
-  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kThreads);
+  const int64_t cap = kWhole ? INT32_MAX : static_cast<int64_t>(sms) * (2048 / kThreads);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
   cfg.blockDim = dim3(kThreads);
@@ -1144,60 +1052,6 @@ int launch(Kernel kernel, int64_t nb, cudaStream_t stream, Args... args) {
   cudaLaunchAttribute attr;
   allow_programmatic_launch(&cfg, &attr);
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MXQ_OK : MXQ_ECUDA;
-}
-
-// The record unpack over nb records (rows of nbl blocks, pitch elements
-// apart): one thread per kRecRuns records, capped at 8 blocks per SM.  The fp32 contiguous form also gets the tensor map of its output and
-// its staging slots in dynamic shared memory (lane stores alone when the map
-// cannot be encoded: rows_y = 0).
-template <bool kBF16, int kFmt, bool kFlat>
-int launch_records(int64_t nb, int64_t nbl, int64_t pitch, const uint8_t* packed, uint8_t* y,
-                   cudaStream_t stream) {
-  const auto kernel = mx_unpack_records_kernel<kBF16, kFmt, kFlat>;
-  const int sms = sm_count_current_device(nullptr);
-  if (sms <= 0) return MXQ_ECUDA;
-  CUtensorMap tm_y{};
-  int64_t rows_y = 0;
-  size_t dyn = 0;
-  if constexpr (rec_tma<kBF16, kFmt, kFlat>()) {
-    // with the static record stage the block uses more than 48 KB of shared
-    // memory, which each device's context must allow once per kernel
-    static std::mutex mu;
-    static bool allowed[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MXQ_ECUDA;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      if (!allowed[dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kRecTmaSmem)) != cudaSuccess)
-          return MXQ_ECUDA;
-        if (MXQ_REC_UNPACK_TMA_CARVEOUT &&
-            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-          return MXQ_ECUDA;
-        allowed[dev] = true;
-      }
-    }
-    dyn = kRecTmaSmem;
-    rows_y = nb / 2;  // 64 output bytes per record
-    if (!encode_rows128_map(&tm_y, y, rows_y, 16)) rows_y = 0;
-  }
-  // as many blocks as 8 per SM, whatever fits at once: measured faster than
-  // one persistent wave of resident blocks (3-6% on every record unpack)
-  const int64_t items = (nb + kRecRuns - 1) / kRecRuns;
-  const int64_t want = (items + kThreads - 1) / kThreads;
-  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kThreads);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = dyn;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  allow_programmatic_launch(&cfg, &attr);
-  return cudaLaunchKernelEx(&cfg, kernel, tm_y, packed, nb, nbl, pitch, y, rows_y) == cudaSuccess
-             ? MXQ_OK
-             : MXQ_ECUDA;
 }
 
 // One thread tests a byte range that starts at the end of a 64-byte dummy
@@ -1264,19 +1118,24 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   uint8_t* yb = static_cast<uint8_t*>(y);
   if (rows_ok(y, dtype, rows, cols, ld, axis, 32 * kRecRuns) && aligned_to(packed, 16)) {
     const int64_t nbl = cols / 16, pitch = rows == 1 ? cols : ld;
-    const bool flat = pitch == cols;
-    if (dtype == MXQ_F32) {
-      if (fmt == MXQ_FMT_MX9)
-        return flat ? launch_records<false, MXQ_FMT_MX9, true>(nb, nbl, pitch, packed, yb, stream)
-                    : launch_records<false, MXQ_FMT_MX9, false>(nb, nbl, pitch, packed, yb, stream);
-      return flat ? launch_records<false, MXQ_FMT_MX6, true>(nb, nbl, pitch, packed, yb, stream)
-                  : launch_records<false, MXQ_FMT_MX6, false>(nb, nbl, pitch, packed, yb, stream);
-    }
-    if (fmt == MXQ_FMT_MX9)
-      return flat ? launch_records<true, MXQ_FMT_MX9, true>(nb, nbl, pitch, packed, yb, stream)
-                  : launch_records<true, MXQ_FMT_MX9, false>(nb, nbl, pitch, packed, yb, stream);
-    return flat ? launch_records<true, MXQ_FMT_MX6, true>(nb, nbl, pitch, packed, yb, stream)
-                : launch_records<true, MXQ_FMT_MX6, false>(nb, nbl, pitch, packed, yb, stream);
+    const int64_t items = (nb + kRecRuns - 1) / kRecRuns;
+    // the whole grid: measured 4-10% faster than 8 blocks per SM walking the
+    // records (16384x8192 / 32768x16384, fraction of the measured copy rate:
+    // MX9 fp32 1.008 / 1.028 against 0.934 / 0.931, MX6 bf16 0.955 / 0.989
+    // against 0.890 / 0.914)
+    auto go = [&](auto flat_kernel, auto strided_kernel) {
+      return pitch == cols ? launch<true>(flat_kernel, items, stream, packed, nb, nbl, pitch, yb)
+                           : launch<true>(strided_kernel, items, stream, packed, nb, nbl, pitch, yb);
+    };
+    if (dtype == MXQ_F32)
+      return fmt == MXQ_FMT_MX9 ? go(mx_unpack_records_kernel<false, MXQ_FMT_MX9, true>,
+                                     mx_unpack_records_kernel<false, MXQ_FMT_MX9, false>)
+                                : go(mx_unpack_records_kernel<false, MXQ_FMT_MX6, true>,
+                                     mx_unpack_records_kernel<false, MXQ_FMT_MX6, false>);
+    return fmt == MXQ_FMT_MX9 ? go(mx_unpack_records_kernel<true, MXQ_FMT_MX9, true>,
+                                   mx_unpack_records_kernel<true, MXQ_FMT_MX9, false>)
+                              : go(mx_unpack_records_kernel<true, MXQ_FMT_MX6, true>,
+                                   mx_unpack_records_kernel<true, MXQ_FMT_MX6, false>);
   }
   const Geometry g{rows, cols, ld};
   if (axis == 0 && cols_tma_ok(y, dtype, fmt, rows, cols, ld, packed, true)) {

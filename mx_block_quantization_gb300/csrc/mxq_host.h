@@ -76,22 +76,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 driver_tensor_map_encoder() {
   return fn;
 }
 
-// A tensor map of `rows` contiguous rows of 128 bytes (32 uint32 words) from
-// `base` (16-byte aligned), box `box_rows` rows, 128-byte swizzle: the form in
-// which the unpack kernels store whole staged runs of output.  False when the
-// driver cannot encode it or a row coordinate would not fit its int32.
-inline bool encode_rows128_map(CUtensorMap* map, void* base, int64_t rows, uint32_t box_rows) {
-  auto enc = driver_tensor_map_encoder();
-  if (!enc || rows < 1 || rows > INT32_MAX) return false;
-  const cuuint64_t dims[2] = {32, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {32, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Number of SMs of the current device, cached per device ordinal.
 inline int sm_count_current_device(int* out_device) {
   static std::atomic<int> cache[64];
