@@ -20,11 +20,11 @@
 // The same kernel writes the packed MX9 / MX6 record forms of mx_packed.cu
 // (blocked rows read at a pitch: one bulk copy per row piece of a stage),
 // staging each warp's 32 records and storing them with one bulk copy.
-// unpack: a streaming kernel, one wave of resident blocks; each lane decodes
-// whole 16-element blocks (exact q * 2^k built without conversion
-// instructions) into a per-warp shared-memory stage, from which a warp's
-// round of 32 blocks leaves as one tensor store (fp32 output) or as 512-byte
-// contiguous lane stores (bf16 output).
+// unpack: a streaming kernel with a warp for every group of 32-block rounds
+// over the whole tensor; each lane decodes whole 16-element blocks (exact
+// q * 2^k built without conversion instructions) into a per-warp
+// shared-memory stage, from which every store instruction writes 512
+// contiguous output bytes.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
