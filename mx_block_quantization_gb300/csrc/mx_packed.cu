@@ -301,15 +301,25 @@ __device__ __forceinline__ float small_int_float(int32_t q) {
   return r;
 }
 
+// Runs of 32 records a warp of the record unpack takes at once, per format
+// and output type.  Measured at 16384x8192 / 32768x16384 (fraction of the
+// measured copy rate): 4 best for MX9 and fp32 (MX9 bf16 0.998 / 1.037 against
+// 0.836 / 0.875 with 8 and 0.956 / 0.986 with 2), 8 for MX6 to bf16 (0.975 /
+// 1.021 against 0.956 / 0.990 with 4).
 #ifndef MXQ_REC_UNPACK_RUNS
 #define MXQ_REC_UNPACK_RUNS 4
 #endif
-constexpr int kRecRuns = MXQ_REC_UNPACK_RUNS;  // runs of 32 records in flight per warp
+#ifndef MXQ_REC_UNPACK_RUNS_MX6_BF16
+#define MXQ_REC_UNPACK_RUNS_MX6_BF16 8
+#endif
+__host__ __device__ constexpr int rec_runs(bool bf16, int fmt) {
+  return bf16 && fmt == MXQ_FMT_MX6 ? MXQ_REC_UNPACK_RUNS_MX6_BF16 : MXQ_REC_UNPACK_RUNS;
+}
 
 // Unpack of a contiguous tensor blocked along its rows: nb records, the
 // output is nb * 16 elements in rows of nbl blocks, ld elements apart (ld ==
-// 16 nbl: one flat run; otherwise nbl >= 32 kRecRuns, so that the records a
-// warp takes at once span at most two rows).  Each warp takes kRecRuns consecutive runs of 32
+// 16 nbl: one flat run; otherwise nbl >= 32 kRuns, so that the records a
+// warp takes at once span at most two rows).  Each warp takes kRuns consecutive runs of 32
 // records at a time: copies them into shared memory with 16-byte loads (all
 // loads issued before the first shared store), then each lane rebuilds 16
 // output bytes (4 fp32 or 8 bf16 elements) at a time, so the stores of a warp
@@ -325,7 +335,8 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int RB = Fmt<kFmt>::kRecord;
   constexpr int kElems = kBF16 ? 8 : 4;  // elements per 16 output bytes
   constexpr int kParts = 16 / kElems;    // output units per block
-  constexpr int kGroup = 32 * kRecRuns;  // records per warp iteration
+  constexpr int kRuns = rec_runs(kBF16, kFmt);
+  constexpr int kGroup = 32 * kRuns;  // records per warp iteration
   constexpr int64_t kEsize = kBF16 ? 2 : 4;
   constexpr int kLoads = (kGroup * RB / 16 + 31) / 32;  // 16-byte loads per lane
   __shared__ __align__(16) uint8_t stage[kWarps][kGroup * kMaxRecord];
@@ -367,7 +378,7 @@ __global__ void __launch_bounds__(kThreads)
     uint8_t* const out0 = y + (row0 * ld + j0 * 16) * kEsize;
     uint8_t* const out1 = y + ((row0 + 1) * ld - (nbl - j0) * 16) * kEsize;
 #pragma unroll
-    for (int j = 0; j < kParts * kRecRuns; ++j) {
+    for (int j = 0; j < kParts * kRuns; ++j) {
       const int u = j * 32 + lane;  // output unit of this group
       const int r = u / kParts, part = u % kParts;
       if (r >= nvalid) continue;
@@ -1116,9 +1127,10 @@ extern "C" int mx_unpack_packed(const uint8_t* packed, int fmt, void* y, int dty
   const int rc = check_args(y, dtype, rows, cols, ld, axis, fmt, packed, &nb);
   if (rc != MXQ_OK || nb == 0) return rc;
   uint8_t* yb = static_cast<uint8_t*>(y);
-  if (rows_ok(y, dtype, rows, cols, ld, axis, 32 * kRecRuns) && aligned_to(packed, 16)) {
+  const int runs = rec_runs(dtype == MXQ_BF16, fmt);
+  if (rows_ok(y, dtype, rows, cols, ld, axis, 32 * runs) && aligned_to(packed, 16)) {
     const int64_t nbl = cols / 16, pitch = rows == 1 ? cols : ld;
-    const int64_t items = (nb + kRecRuns - 1) / kRecRuns;
+    const int64_t items = (nb + runs - 1) / runs;
     // the whole grid: measured 4-10% faster than 8 blocks per SM walking the
     // records (16384x8192 / 32768x16384, fraction of the measured copy rate:
     // MX9 fp32 1.008 / 1.028 against 0.934 / 0.931, MX6 bf16 0.955 / 0.989
